@@ -1,0 +1,108 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) tiled online-softmax attention forward pass.
+ *
+ * The operation (aiml.sh "Speed up long contexts with FlashAttention", lab.py:
+ * `standard_attention` defines the result, `tiled_flash_attention` the blocked
+ * online-softmax method that reaches it without holding the N x N matrix):
+ *
+ *     for every head h of every batch b and every query row i < N
+ *       s_j   = scale * <q[b,h,i,:], k[b,h,j,:]>      j in J_i
+ *       J_i   = {0..i} when causal (query i sees keys j <= i), else {0..N-1}
+ *       o[b,h,i,:] = sum_j softmax(s)_j * v[b,h,j,:]
+ *       lse[b,h,i] = ln( sum_j exp(s_j) )             (natural-log logsumexp)
+ *
+ * computed tile by tile: a running row maximum, a running sum and an accumulator
+ * rescaled when the maximum grows, so the score matrix never reaches device memory.
+ * The logsumexp output is not on the pages; it is the plain definition above.
+ *
+ * All functions are plain C, take raw pointers and sizes, and never allocate
+ * device memory.  Compute is asynchronous on the caller's stream.
+ */
+#ifndef FA_SM103_H
+#define FA_SM103_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, non-finite or negative scale, aliasing */
+    FA_ERR_UNSUPPORTED = 2,    /* head dim not in {16, 32, 64, 128}, or a size beyond the kernel's range */
+    FA_ERR_MISALIGNED = 3,     /* a tensor base address not 16-byte aligned (lse: 4-byte) */
+    FA_ERR_ARCH = 4,           /* current device is not compute capability 10.3 (sm_103) */
+    FA_ERR_CUDA = 5,           /* a CUDA runtime / driver call failed; see fa_last_error() */
+    FA_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait ran out (reported by fa_get_device_status) */
+} fa_status;
+
+/*
+ * fa_fwd -- attention forward pass.
+ *
+ *   q, k, v  device pointers, bf16, shape [B, H, N, d], contiguous row-major
+ *            (d fastest), 16-byte aligned.  Read only.  q, k and v may alias.
+ *   o        device pointer, bf16, [B, H, N, d] contiguous, 16-byte aligned.
+ *            Written: o = softmax(scale q k^T + mask) v, rounded to bf16 (nearest even).
+ *   lse      device pointer, fp32, [B, H, N] contiguous, or NULL to skip it.
+ *   B, H, N  batch, heads, sequence length (queries = keys = N).  B*H*N == 0 is a no-op.
+ *   d        head dimension, one of 16, 32, 64, 128.
+ *   causal   nonzero: query i attends keys j <= i (top-left aligned square mask).
+ *   scale    finite, >= 0 (usually 1/sqrt(d)); applied to q.k before the softmax.
+ *   stream   cudaStream_t to launch on (NULL = the legacy default stream).
+ *
+ * Ownership: the caller owns every buffer and keeps it alive until the stream's
+ * work completes; the library keeps no pointer after returning.  o and lse must
+ * not overlap q, k, v or each other.  Every argument is checked before any launch;
+ * on an error nothing is launched and nothing is written.  The call itself does not
+ * synchronise; a device-side wait that ran out is reported later by
+ * fa_get_device_status().
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+           void* stream);
+
+/*
+ * Options for fa_fwd_opts (zero-initialise, then set what you need).
+ *   wait_budget_cycles  cap, in SM clock cycles, on any single wait inside the kernel
+ *                       (0 = default, about one second).  A wait that runs out ends
+ *                       the kernel's work early and raises FA_ERR_DEVICE_TIMEOUT.
+ *   inject_skip_kv_load test hook: when > 0, work unit 0 never issues its
+ *                       (inject_skip_kv_load)-th K/V tile load, so the consumer's
+ *                       bounded wait must run out (host-side fault injection; no
+ *                       GPU fault is involved).  0 = off.
+ *   max_ctas            cap on the persistent grid (0 = one CTA per SM).
+ */
+typedef struct {
+    int64_t wait_budget_cycles;
+    int32_t inject_skip_kv_load;
+    int32_t max_ctas;
+} fa_fwd_options;
+
+/* fa_fwd with options; opts may be NULL (same as fa_fwd). */
+int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse,
+                int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                void* stream, const fa_fwd_options* opts);
+
+/* Static description of a status code. Never NULL. */
+const char* fa_strerror(int status);
+
+/* Detail of the last error on this host thread ("" if the last call succeeded). */
+const char* fa_last_error(void);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT if a kernel on this device gave up a wait
+ * since the last call, or FA_ERR_CUDA if the synchronisation itself failed.
+ */
+int fa_get_device_status(void* stream);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_SM103_H */

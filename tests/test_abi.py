@@ -1,0 +1,91 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function ``include/fa.h`` declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tiled_online_softmax_fa_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            with open(os.path.join(inc, fn)) as f:
+                text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+            names |= set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_builds_and_loads():
+    lib = fa.load_library()
+    assert isinstance(lib, ctypes.CDLL)
+    assert fa.version() == 100
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared_functions()
+    assert {"fa_fwd", "fa_fwd_opts", "fa_strerror", "fa_last_error", "fa_get_device_status",
+            "fa_version"} <= set(names)
+    lib = fa.load_library()
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_strerror_covers_every_status():
+    for code in range(7):
+        assert fa.strerror(code) and fa.strerror(code) != "unknown status"
+    assert fa.strerror(99) == "unknown status"
+
+
+def _call(**kw):
+    args = dict(q_ptr=0x10000, k_ptr=0x20000, v_ptr=0x30000, o_ptr=0x40000, lse_ptr=0,
+                B=1, H=1, N=128, d=64, causal=True, scale=0.125)
+    args.update(kw)
+    return fa.fa_fwd_raw(**args)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(B=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(N=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(d=48), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(q_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(o_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_INVALID_ARG),
+    (dict(q_ptr=0x10008), fa.FA_ERR_MISALIGNED),
+    (dict(o_ptr=0x40002), fa.FA_ERR_MISALIGNED),
+    (dict(lse_ptr=0x50002), fa.FA_ERR_MISALIGNED),
+    (dict(o_ptr=0x10000 + 4096), fa.FA_ERR_INVALID_ARG),          # o overlaps q
+    (dict(lse_ptr=0x40000 + 64), fa.FA_ERR_INVALID_ARG),          # lse overlaps o
+    (dict(N=(1 << 30) + 1), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=1 << 20, H=1 << 12), fa.FA_ERR_UNSUPPORTED),
+])
+def test_argument_errors(kw, want):
+    assert _call(**kw) == want
+    assert fa.last_error() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(N=0),
+                                dict(B=0, q_ptr=0, k_ptr=0, v_ptr=0, o_ptr=0)])
+def test_empty_is_a_noop_without_cuda(kw):
+    assert _call(**kw) == fa.FA_OK
+
+
+def test_options_are_checked():
+    opts = fa.FwdOptions(wait_budget_cycles=-1)
+    assert _call(options=opts) == fa.FA_ERR_INVALID_ARG
+
+
+def test_python_wrapper_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    t = torch.zeros((1, 1, 8, 16), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        fa.fa_fwd(t, t, t)

@@ -1,0 +1,148 @@
+"""Python binding of the GB300 (sm_103a) attention forward library.
+
+Argument marshalling only: every step of the computation runs in the CUDA kernel
+behind the C ABI of ``include/fa.h``.  PyTorch supplies device memory and the
+stream.  There is no fallback: if the compiled library cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+
+from . import build as _build
+
+__all__ = ["fa_fwd", "fa_fwd_raw", "get_device_status", "strerror", "last_error", "version",
+           "load_library", "FAError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED",
+           "FA_ERR_MISALIGNED", "FA_ERR_ARCH", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
+           "FwdOptions", "SUPPORTED_HEAD_DIMS"]
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_ARCH = 4
+FA_ERR_CUDA = 5
+FA_ERR_DEVICE_TIMEOUT = 6
+SUPPORTED_HEAD_DIMS = (16, 32, 64, 128)
+
+
+class FwdOptions(ctypes.Structure):
+    """Mirror of ``fa_fwd_options``."""
+    _fields_ = [("wait_budget_cycles", ctypes.c_int64),
+                ("inject_skip_kv_load", ctypes.c_int32),
+                ("max_ctas", ctypes.c_int32)]
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = last_error()
+        super().__init__(f"{where}: {strerror(status)} (status {status})"
+                         + (f": {detail}" if detail else ""))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libfa_sm103.so."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB_PATH
+        lib = ctypes.CDLL(path)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        sig = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp]
+        lib.fa_fwd.argtypes = sig
+        lib.fa_fwd.restype = ctypes.c_int
+        lib.fa_fwd_opts.argtypes = sig + [ctypes.POINTER(FwdOptions)]
+        lib.fa_fwd_opts.restype = ctypes.c_int
+        lib.fa_strerror.argtypes = [ctypes.c_int]
+        lib.fa_strerror.restype = ctypes.c_char_p
+        lib.fa_last_error.argtypes = []
+        lib.fa_last_error.restype = ctypes.c_char_p
+        lib.fa_get_device_status.argtypes = [vp]
+        lib.fa_get_device_status.restype = ctypes.c_int
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def strerror(status: int) -> str:
+    return load_library().fa_strerror(int(status)).decode()
+
+
+def last_error() -> str:
+    return load_library().fa_last_error().decode()
+
+
+def version() -> int:
+    return int(load_library().fa_version())
+
+
+def fa_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+               N: int, d: int, causal: bool, scale: float, stream: int = 0,
+               options: FwdOptions | None = None) -> int:
+    """Call the C entry point with raw device addresses; returns the status code."""
+    lib = load_library()
+    args = (q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None, lse_ptr or None,
+            int(B), int(H), int(N), int(d), int(bool(causal)), float(scale), stream or None)
+    if options is None:
+        return int(lib.fa_fwd(*args))
+    return int(lib.fa_fwd_opts(*args, ctypes.byref(options)))
+
+
+def _stream_handle(stream, device) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def fa_fwd(q, k, v, o=None, lse=None, causal: bool = True, scale: float | None = None,
+           want_lse: bool = True, stream=None, options: FwdOptions | None = None):
+    """O = softmax(scale * q k^T + mask) v and its row logsumexp, on the GPU.
+
+    q, k, v : CUDA bf16 tensors [B, H, N, d], contiguous, d in {16, 32, 64, 128}.
+    o, lse  : optional outputs ([B, H, N, d] bf16, [B, H, N] fp32); allocated if None.
+    scale   : defaults to 1/sqrt(d), rounded to fp32.
+    Returns (o, lse) (lse is None when ``want_lse`` is False and none was given).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a CUDA bf16 tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    if o is None:
+        o = torch.empty_like(q)
+    elif o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous() or not o.is_cuda:
+        raise ValueError("o must be a contiguous CUDA bf16 tensor shaped like q")
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif lse is not None and (tuple(lse.shape) != (B, H, N) or lse.dtype != torch.float32
+                              or not lse.is_contiguous() or not lse.is_cuda):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor [B, H, N]")
+    rc = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                    lse.data_ptr() if lse is not None else 0, B, H, N, d, causal, scale,
+                    _stream_handle(stream, q.device), options)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd")
+    return o, lse
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status (FA_OK or a timeout)."""
+    import torch
+    handle = _stream_handle(stream, torch.cuda.current_device())
+    return int(load_library().fa_get_device_status(handle or None))

@@ -1,0 +1,247 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument checks, TMA
+// tensor-map encoding, the persistent launch and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultBudget = 2000000000LL;  // ~1 s of SM clock
+
+thread_local std::string t_last_error;
+
+int set_error(int status, const std::string& msg) {
+  t_last_error = msg;
+  return status;
+}
+
+int cuda_error(const char* what, cudaError_t e) {
+  return set_error(FA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// cuTensorMapEncodeTiled, fetched through the runtime so the library needs no -lcuda
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool probed = false;
+  bool arch_ok = false;
+  int num_sms = 0;
+  bool smem_set[4] = {false, false, false, false};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+int head_dim_index(int64_t d) {
+  switch (d) {
+    case 16: return 0;
+    case 32: return 1;
+    case 64: return 2;
+    case 128: return 3;
+    default: return -1;
+  }
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Encode a [BH, N, d] bf16 tensor as a 3-D tiled map with a (W x 128 x 1) box.
+int encode_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t d) {
+  const int w = d < 64 ? static_cast<int>(d) : 64;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
+                                 static_cast<cuuint64_t>(N * d * 2)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(w), fa_sm103::kBlockM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = w * 2 == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : w * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return set_error(FA_ERR_CUDA, buf);
+  }
+  return FA_OK;
+}
+
+template <int HD>
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
+           int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
+           bool& smem_set, const fa_fwd_options* opts) {
+  using C = fa_sm103::Cfg<HD>;
+  CUtensorMap mq, mk, mv;
+  int st;
+  if ((st = encode_map(&mq, q, BH, N, HD)) != FA_OK) return st;
+  if ((st = encode_map(&mk, k, BH, N, HD)) != FA_OK) return st;
+  if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
+  if (!smem_set) {
+    const cudaError_t e = cudaFuncSetAttribute(fa_sm103::fa_fwd_kernel<HD>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               C::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
+    smem_set = true;
+  }
+  fa_sm103::Params p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = static_cast<int>(BH);
+  p.N = static_cast<int>(N);
+  p.nkv = static_cast<int>((N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN);
+  p.nqb = static_cast<int>((N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows);
+  p.num_units = static_cast<int>(static_cast<int64_t>(p.nqb) * BH);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.budget = (opts && opts->wait_budget_cycles > 0) ? opts->wait_budget_cycles : kDefaultBudget;
+  p.inject = opts ? opts->inject_skip_kv_load : 0;
+  int grid = dev.num_sms;
+  if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
+  if (grid > p.num_units) grid = p.num_units;
+  fa_sm103::fa_fwd_kernel<HD><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error("kernel launch", e);
+  return FA_OK;
+}
+
+// Per-device facts, probed once: architecture and SM count.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return set_error(FA_ERR_UNSUPPORTED, "device index too large");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_error("cudaDeviceGetAttribute", e);
+    s.arch_ok = (major == 10 && minor == 3);
+    s.num_sms = sms;
+    s.probed = true;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qr);
+    if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn)
+      return set_error(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = &s;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                int64_t H, int64_t N, int64_t d, int causal, float scale, void* stream,
+                const fa_fwd_options* opts) {
+  t_last_error.clear();
+  // ---- pure argument checks: no CUDA call before these pass ----
+  if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
+  const int hd = head_dim_index(d);
+  if (hd < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128");
+  if (B == 0 || H == 0 || N == 0) return FA_OK;  // nothing to compute
+  if (!q || !k || !v || !o) return set_error(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return set_error(FA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  if (B > INT32_MAX / H) return set_error(FA_ERR_UNSUPPORTED, "B*H too large");
+  const int64_t BH = B * H;
+  if (N > (int64_t{1} << 30)) return set_error(FA_ERR_UNSUPPORTED, "N too large");
+  const int64_t units = ((N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows) * BH;
+  if (units > INT32_MAX) return set_error(FA_ERR_UNSUPPORTED, "too many work units");
+  if (BH > (INT64_MAX / 4) / (N * d)) return set_error(FA_ERR_UNSUPPORTED, "tensor too large");
+  const size_t bytes = static_cast<size_t>(BH * N * d) * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH * N) * 4;
+  for (const void* ptr : {q, k, v, static_cast<const void*>(o)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+      return set_error(FA_ERR_MISALIGNED, "tensor base address not 16-byte aligned");
+  if (lse && reinterpret_cast<uintptr_t>(lse) % 4 != 0)
+    return set_error(FA_ERR_MISALIGNED, "lse not 4-byte aligned");
+  for (const void* in : {q, k, v}) {
+    if (overlaps(o, bytes, in, bytes)) return set_error(FA_ERR_INVALID_ARG, "o overlaps an input");
+    if (lse && overlaps(lse, lse_bytes, in, bytes))
+      return set_error(FA_ERR_INVALID_ARG, "lse overlaps an input");
+  }
+  if (lse && overlaps(lse, lse_bytes, o, bytes)) return set_error(FA_ERR_INVALID_ARG, "lse overlaps o");
+  if (opts && (opts->wait_budget_cycles < 0 || opts->inject_skip_kv_load < 0 || opts->max_ctas < 0))
+    return set_error(FA_ERR_INVALID_ARG, "negative option");
+
+  // ---- device checks ----
+  DeviceState* dev = nullptr;
+  int st = device_state(&dev);
+  if (st != FA_OK) return st;
+  if (!dev->arch_ok) return set_error(FA_ERR_ARCH, "device is not sm_103 (GB300-class)");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool& smem_set = dev->smem_set[hd];
+  switch (hd) {
+    case 0: return launch<16>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
+    case 1: return launch<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
+    case 2: return launch<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
+    default: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+           int64_t N, int64_t d, int causal, float scale, void* stream) {
+  return fa_fwd_opts(q, k, v, o, lse, B, H, N, d, causal, scale, stream, nullptr);
+}
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "success";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported size or head dimension";
+    case FA_ERR_MISALIGNED: return "misaligned pointer";
+    case FA_ERR_ARCH: return "device is not sm_103";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_DEVICE_TIMEOUT: return "a kernel wait ran out of time";
+    default: return "unknown status";
+  }
+}
+
+const char* fa_last_error(void) { return t_last_error.c_str(); }
+
+int fa_get_device_status(void* stream) {
+  t_last_error.clear();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error("cudaStreamSynchronize", e);
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, fa_sm103::g_device_status, sizeof word);
+  if (e != cudaSuccess) return cuda_error("cudaMemcpyFromSymbol", e);
+  if (word == 0) return FA_OK;
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(fa_sm103::g_device_status, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_error("cudaMemcpyToSymbol", e);
+  return FA_ERR_DEVICE_TIMEOUT;
+}
+
+int fa_version(void) { return kVersion; }
+
+}  // extern "C"

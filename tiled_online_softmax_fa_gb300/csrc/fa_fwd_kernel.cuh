@@ -1,0 +1,509 @@
+// fa_fwd_kernel.cuh -- the sm_103a attention forward kernel.
+//
+// Method: the blocked online softmax of aiml.sh "Speed up long contexts with
+// FlashAttention" (lab.py, `tiled_flash_attention`): per query row a running maximum
+// m, a running sum l and an accumulator rescaled by exp(m_old - m_new) when m grows,
+// finished by O = acc / l.  Causal key blocks entirely above the diagonal are never
+// visited and the diagonal block is masked (j <= i).
+//
+// GB300 mapping (not from the pages; designed for sm_103a):
+//   * Work unit = one (batch*head, 256-query-row block) = two 128-row Q tiles that
+//     share every K/V tile.  Persistent CTAs (one per SM) walk the units in a static
+//     round-robin over a longest-first order (causal units shrink with the block index).
+//   * Warp roles (384 threads = 3 warpgroups): warps 0-3 = softmax for Q tile 0,
+//     warps 4-7 = softmax for Q tile 1 (one thread per query row), warp 8 = tcgen05
+//     MMA issuer (one lane), warp 9 = TMA producer (one lane), warps 10-11 idle.  The
+//     launch gives 168 registers a thread; the control warpgroup drops to 88 and the
+//     softmax warpgroups rise to 208 (208*256 + 88*128 = 168*384).
+//   * Shared memory: Q0, Q1 pinned for the unit; K and V tiles stream through an
+//     NSLOT-deep ring of 128-row slots filled by TMA (128/64/32-byte swizzle).
+//   * Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
+//     softmax writes P (bf16, two per column) over the first 64 columns of its S.
+//   * MMA order per KV tile j: PV0(j), S0(j+1), PV1(j), S1(j+1).  tcgen05 MMAs from
+//     one thread run in issue order, so when S_t(j+1) is complete PV_t(j) is too: the
+//     softmax may then rescale O_t in place before publishing P_t(j+1).
+//   * Lazy rescale: the reference maximum m_ref (log2 units) only moves when a tile's
+//     maximum exceeds it by more than kRescaleLog2, so P <= 2^kRescaleLog2 and O is
+//     rarely touched.  Two running sums: l_exact (fp32 P, for the logsumexp) and
+//     l_round (the bf16-rounded P the MMA multiplies by V, used to normalise O so
+//     the weights of every output row sum to one exactly as applied).
+//   * Every mbarrier wait is bounded; a wait that runs out sets the CTA's abort flag
+//     and the device status word, and every role then winds down without hanging.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx_sm103.cuh"
+
+namespace fa_sm103 {
+
+// bit 0: a bounded wait inside the kernel ran out
+__device__ unsigned int g_device_status;
+
+constexpr int kBlockM = 128;                // query rows per Q tile (TMEM lanes)
+constexpr int kBlockN = 128;                // keys per K/V tile
+constexpr int kUnitRows = 2 * kBlockM;      // query rows per work unit
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsSoftmax = 208;      // per thread, warpgroups 0 and 1
+constexpr uint32_t kRegsControl = 88;       // per thread, warpgroup 2
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+constexpr float kRescaleLog2 = 8.0f;        // lazy-rescale threshold, log2 units
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int HD>
+struct Cfg {
+  static_assert(HD == 16 || HD == 32 || HD == 64 || HD == 128, "head dim");
+  static constexpr int W = HD < 64 ? HD : 64;          // elements per swizzled smem row
+  static constexpr int SWB = 2 * W;                     // bytes per swizzled smem row
+  static constexpr int NCH = HD / W;                    // row chunks across the head dim
+  static constexpr int TILE_BYTES = kBlockM * HD * 2;   // one 128-row bf16 tile
+  static constexpr int CHUNK_BYTES = kBlockM * SWB;     // one chunk of a tile
+  static constexpr int NSLOT = HD == 128 ? 4 : 8;       // K/V ring depth
+  static constexpr int SMEM_Q = 2 * TILE_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_Q + NSLOT * TILE_BYTES + 1024;  // + alignment pad
+  static constexpr uint32_t SWZ = swizzle_code(SWB);
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(kBlockM, kBlockN, false);
+  static constexpr uint32_t IDESC_O = idesc_bf16_f32(kBlockM, HD, true);
+};
+
+struct Params {
+  __nv_bfloat16* o;   // [BH, N, HD]
+  float* lse;         // [BH, N] or null
+  int BH;             // batch * heads
+  int N;              // sequence length
+  int nkv;            // ceil(N / 128)
+  int nqb;            // ceil(N / 256)
+  int num_units;      // nqb * BH
+  int causal;
+  float scale_log2;   // scale * log2(e), >= 0
+  long long budget;   // cycles a single wait may take
+  int inject;         // > 0: unit 0 never issues its inject-th K/V ring load
+};
+
+struct Barriers {
+  uint64_t q_full, q_empty, drain;
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t slot_full[8], slot_empty[8];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void unit_coords(int u, const Params& p, int& bh, int& row0) {
+  const int qb = p.nqb - 1 - u / p.BH;  // longest causal units first
+  bh = u % p.BH;
+  row0 = qb * kUnitRows;
+}
+
+// Number of K/V tiles a Q tile starting at `row_start` visits (0 if it holds no row < N).
+__device__ __forceinline__ int tiles_for(int row_start, const Params& p) {
+  if (row_start >= p.N) return 0;
+  if (!p.causal) return p.nkv;
+  const int t = row_start / kBlockN + 1;  // tiles up to and including the diagonal one
+  return t < p.nkv ? t : p.nkv;
+}
+
+__device__ __forceinline__ void raise_abort(Barriers& b) {
+  *reinterpret_cast<volatile int*>(&b.abort) = 1;
+  atomicOr(&g_device_status, 1u);
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p,
+                                         Barriers& b) {
+  return mbar_wait_bounded(bar, parity, p.budget, &b.abort);
+}
+
+// Time-bounded wait that ignores the abort flag (used to drain in-flight async work).
+__device__ __forceinline__ bool drain_bar(uint64_t* bar, uint32_t parity, const Params& p) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > p.budget) return false;
+  return true;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* ptr) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+  return reinterpret_cast<uint8_t*>((a + 1023) & ~uintptr_t(1023));
+}
+
+// ------------------------------------------------------------------------------------
+// TMA producer (one lane)
+// ------------------------------------------------------------------------------------
+template <int HD>
+__device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                          uint8_t* sQ, uint8_t* sRing, Barriers& b, const Params& p) {
+  using C = Cfg<HD>;
+  prefetch_tmap(tmQ);
+  prefetch_tmap(tmK);
+  prefetch_tmap(tmV);
+  uint32_t ring = 0;          // K/V ring entries issued so far
+  uint32_t units = 0;         // units whose Q was issued
+  uint32_t skipped = 0xFFFFFFFFu;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, row0;
+    unit_coords(u, p, bh, row0);
+    const int n0 = tiles_for(row0, p), n1 = tiles_for(row0 + kBlockM, p);
+    const int n = n0 > n1 ? n0 : n1;
+    // Q smem is free once the previous unit's last S MMA has completed
+    if (units > 0 && !wait_bar(&b.q_empty, (units - 1) & 1, p, b)) goto fail;
+    mbar_arrive_expect_tx(&b.q_full, 2 * C::TILE_BYTES);
+    for (int t = 0; t < 2; ++t)
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, tmQ, &b.q_full, c * C::W,
+                    row0 + t * kBlockM, bh);
+    ++units;
+    for (int j = 0; j < n; ++j) {
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint32_t slot = ring % C::NSLOT, round = ring / C::NSLOT;
+        if (round > 0 && !wait_bar(&b.slot_empty[slot], (round - 1) & 1, p, b)) goto fail;
+        const bool skip = p.inject > 0 && u == 0 && ring + 1 == static_cast<uint32_t>(p.inject);
+        if (skip) {
+          skipped = ring;
+        } else {
+          mbar_arrive_expect_tx(&b.slot_full[slot], C::TILE_BYTES);
+          const CUtensorMap* m = kv == 0 ? tmK : tmV;
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sRing + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, m, &b.slot_full[slot],
+                        c * C::W, j * kBlockN, bh);
+        }
+        ++ring;
+      }
+    }
+  }
+  goto drain;
+fail:
+  raise_abort(b);
+drain:
+  // let every load this CTA issued land before shared memory is released
+  for (uint32_t i = ring > C::NSLOT ? ring - C::NSLOT : 0; i < ring; ++i)
+    if (i != skipped) drain_bar(&b.slot_full[i % C::NSLOT], (i / C::NSLOT) & 1, p);
+  if (units > 0) drain_bar(&b.q_full, (units - 1) & 1, p);
+}
+
+// ------------------------------------------------------------------------------------
+// MMA issuer (one lane)
+// ------------------------------------------------------------------------------------
+template <int HD>
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_addr, uint32_t k_addr) {
+  using C = Cfg<HD>;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const int ch = (kk * 16) / C::W, off = ((kk * 16) % C::W) * 2;
+    const uint64_t a = smem_desc(q_addr + ch * C::CHUNK_BYTES + off, 16, 8 * C::SWB, C::SWZ);
+    const uint64_t bd = smem_desc(k_addr + ch * C::CHUNK_BYTES + off, 16, 8 * C::SWB, C::SWZ);
+    mma_bf16_ss(tmem_d, a, bd, C::IDESC_S, kk > 0);
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
+                                         bool accumulate) {
+  using C = Cfg<HD>;
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+    // V tile is [key][d]: the B operand (K = keys, N = d) is MN-major
+    const uint64_t bd = smem_desc(v_addr + kk * 16 * C::SWB, C::CHUNK_BYTES, 8 * C::SWB, C::SWZ);
+    mma_bf16_ts(tmem_o, tmem_p + kk * 8, bd, C::IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int HD>
+__device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b, const Params& p) {
+  using C = Cfg<HD>;
+  uint32_t ring = 0, units = 0;
+  uint32_t p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
+  const uint32_t q_addr[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE_BYTES)};
+  const uint32_t col_s[2] = {kColS0, kColS1}, col_o[2] = {kColO0, kColO1};
+  const uint32_t ring_addr = smem_u32(sRing);
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, row0;
+    unit_coords(u, p, bh, row0);
+    const int nt[2] = {tiles_for(row0, p), tiles_for(row0 + kBlockM, p)};
+    const int n = nt[0] > nt[1] ? nt[0] : nt[1];
+    if (!wait_bar(&b.q_full, units & 1, p, b)) goto fail;
+    ++units;
+    uint32_t ks = ring % C::NSLOT;
+    if (!wait_bar(&b.slot_full[ks], (ring / C::NSLOT) & 1, p, b)) goto fail;
+    ++ring;
+    tc_fence_after_sync();
+    for (int t = 0; t < 2; ++t)
+      if (nt[t] > 0) {
+        issue_s<HD>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::TILE_BYTES);
+        mma_commit(&b.s_full[t]);
+      }
+    mma_commit(&b.slot_empty[ks]);
+    if (n == 1) mma_commit(&b.q_empty);
+    for (int j = 0; j < n; ++j) {
+      const uint32_t vs = ring % C::NSLOT;
+      if (!wait_bar(&b.slot_full[vs], (ring / C::NSLOT) & 1, p, b)) goto fail;
+      ++ring;
+      const bool next = j + 1 < n;
+      if (next) {
+        ks = ring % C::NSLOT;
+        if (!wait_bar(&b.slot_full[ks], (ring / C::NSLOT) & 1, p, b)) goto fail;
+        ++ring;
+      }
+      tc_fence_after_sync();
+      for (int t = 0; t < 2; ++t) {
+        if (j < nt[t]) {
+          if (j == 0) {  // O_t must have been read out by the previous unit's epilogue
+            if (!wait_bar(&b.o_empty[t], (oe_cnt[t] & 1) ^ 1, p, b)) goto fail;
+            ++oe_cnt[t];
+          }
+          if (!wait_bar(&b.p_full[t], p_cnt[t] & 1, p, b)) goto fail;
+          ++p_cnt[t];
+          tc_fence_after_sync();
+          issue_pv<HD>(tmem + col_o[t], tmem + col_s[t], ring_addr + vs * C::TILE_BYTES, j > 0);
+          if (j == nt[t] - 1) mma_commit(&b.o_full[t]);
+        }
+        if (next && j + 1 < nt[t]) {
+          issue_s<HD>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::TILE_BYTES);
+          mma_commit(&b.s_full[t]);
+        }
+      }
+      mma_commit(&b.slot_empty[vs]);
+      if (next) {
+        mma_commit(&b.slot_empty[ks]);
+        if (j + 1 == n - 1) mma_commit(&b.q_empty);
+      }
+    }
+  }
+  goto drain;
+fail:
+  raise_abort(b);
+drain:
+  // every MMA this thread issued has completed once this commit arrives
+  mma_commit(&b.drain);
+  drain_bar(&b.drain, 0, p);
+}
+
+// ------------------------------------------------------------------------------------
+// softmax / epilogue (warps 0-7, one thread per query row)
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
+                                          Barriers& b) {
+  const bool ok = wait_bar(bar, parity, p, b);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// `half` selects columns [64*half, 64*half + 64); the 32 packed words go to pk.
+// Returns {sum of the exact fp32 P, sum of the bf16-rounded P}.
+template <bool MASK>
+__device__ __forceinline__ float2 exp_pack_half(const uint32_t (&s)[128], uint32_t (&pk)[32],
+                                                int half, float c, float neg_m, int lim) {
+  float e0 = 0.f, e1 = 0.f, r0 = 0.f, r1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int col = 64 * half + 2 * i;
+    float p0 = ex2_approx(fmaf(__uint_as_float(s[col]), c, neg_m));
+    float p1 = ex2_approx(fmaf(__uint_as_float(s[col + 1]), c, neg_m));
+    if (MASK) {
+      if (col > lim) p0 = 0.f;
+      if (col + 1 > lim) p1 = 0.f;
+    }
+    const uint32_t w = pack_bf16x2(p0, p1);
+    pk[i] = w;
+    e0 += p0;
+    e1 += p1;
+    r0 += __uint_as_float(w << 16);
+    r1 += __uint_as_float(w & 0xFFFF0000u);
+  }
+  return make_float2(e0 + e1, r0 + r1);
+}
+
+template <bool MASK>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[128], int lim) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 128; i += 4) {
+    float x0 = __uint_as_float(s[i]), x1 = __uint_as_float(s[i + 1]);
+    float x2 = __uint_as_float(s[i + 2]), x3 = __uint_as_float(s[i + 3]);
+    if (MASK) {
+      if (i > lim) x0 = -INFINITY;
+      if (i + 1 > lim) x1 = -INFINITY;
+      if (i + 2 > lim) x2 = -INFINITY;
+      if (i + 3 > lim) x3 = -INFINITY;
+    }
+    m0 = fmaxf(m0, x0);
+    m1 = fmaxf(m1, x1);
+    m2 = fmaxf(m2, x2);
+    m3 = fmaxf(m3, x3);
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+template <int HD>
+__device__ void softmax_role(uint32_t tmem, Barriers& b, const Params& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = warp >> 2, wq = warp & 3;
+  const int lrow = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_base + (t == 0 ? kColS0 : kColS1);
+  const uint32_t tO = tmem + lane_base + (t == 0 ? kColO0 : kColO1);
+  const float c = p.scale_log2;
+  uint32_t s_cnt = 0, o_cnt = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int bh, row0;
+    unit_coords(u, p, bh, row0);
+    const int row_start = row0 + t * kBlockM;
+    const int nt = tiles_for(row_start, p);
+    if (nt == 0) continue;
+    const int row = row_start + lrow;
+    // admissible keys for this row: j <= last_key
+    const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
+    float m_ref = -INFINITY;  // reference maximum, log2 units
+    float l_exact = 0.f, l_round = 0.f;
+    for (int j = 0; j < nt; ++j) {
+      if (!warp_wait(&b.s_full[t], s_cnt & 1, p, b)) goto fail;
+      ++s_cnt;
+      tc_fence_after_sync();
+      uint32_t s[128];
+      tmem_ld_x128(tS, s);
+      tmem_wait_ld(s);
+      const int kv0 = j * kBlockN;
+      const int lim = last_key - kv0;               // last admissible column in this tile
+      const bool mask = (kv0 + kBlockN - 1 > last_key);
+      const bool warp_mask = __any_sync(0xFFFFFFFFu, mask);
+      const float mx = warp_mask ? row_max<true>(s, lim) : row_max<false>(s, lim);
+      const float mt = mx * c;
+      const bool need = mt > m_ref + kRescaleLog2;  // also true while m_ref is -inf
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        float alpha = 1.f;
+        if (need) {
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
+          m_ref = mt;
+          l_exact *= alpha;
+          l_round *= alpha;
+        }
+        if (j > 0) {
+          // PV_t(j-1) has completed (S_t(j) was issued after it): rescale O_t in place
+#pragma unroll
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c0, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_x32(tO + c0, o);
+          }
+        }
+      }
+      const float neg_m = -m_ref;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+        const float2 sums = warp_mask ? exp_pack_half<true>(s, pk, half, c, neg_m, lim)
+                                      : exp_pack_half<false>(s, pk, half, c, neg_m, lim);
+        l_exact += sums.x;
+        l_round += sums.y;
+        tmem_st_x32(tS + 32 * half, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(&b.p_full[t]);
+    }
+    // epilogue: O = acc / l_round in bf16, lse = (m_ref + log2 l_exact) ln 2
+    if (!warp_wait(&b.o_full[t], o_cnt & 1, p, b)) goto fail;
+    ++o_cnt;
+    tc_fence_after_sync();
+    {
+      const float inv_l = 1.f / l_round;
+      const bool store = row < p.N;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + row) * HD;
+#pragma unroll
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + c0, o);
+        tmem_wait_ld(o);
+        if (store) {
+          constexpr int NV = HD < 32 ? HD : 32;
+#pragma unroll
+          for (int v8 = 0; v8 < NV; v8 += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[v8 + 0]) * inv_l, __uint_as_float(o[v8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[v8 + 2]) * inv_l, __uint_as_float(o[v8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[v8 + 4]) * inv_l, __uint_as_float(o[v8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[v8 + 6]) * inv_l, __uint_as_float(o[v8 + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + c0 + v8) = w;
+          }
+        }
+      }
+      if (store && p.lse != nullptr)
+        p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + lg2_approx(l_exact)) * kLn2;
+    }
+    tc_fence_before_sync();
+    mbar_arrive(&b.o_empty[t]);
+  }
+  return;
+fail:
+  raise_abort(b);
+}
+
+// ------------------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::SMEM_Q;
+  __shared__ Barriers b;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    b.abort = 0;
+    mbar_init(&b.q_full, 1);
+    mbar_init(&b.q_empty, 1);
+    mbar_init(&b.drain, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&b.s_full[t], 1);
+      mbar_init(&b.p_full[t], kBlockM);
+      mbar_init(&b.o_full[t], 1);
+      mbar_init(&b.o_empty[t], kBlockM);
+    }
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&b.slot_full[s], 1);
+      mbar_init(&b.slot_empty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&b.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = b.tmem_base;
+
+  if (warp < 8) {
+    setmaxnreg_inc<kRegsSoftmax>();
+    softmax_role<HD>(tmem, b, p);
+  } else {
+    setmaxnreg_dec<kRegsControl>();
+    if (warp == kMmaWarp) {
+      if (lane == 0) mma_role<HD>(sQ, sRing, tmem, b, p);
+      __syncwarp();
+    } else if (warp == kLoadWarp) {
+      if (lane == 0) load_role<HD>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa_sm103
