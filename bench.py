@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the sm_103a attention forward pass.
+
+Workload (one step = one fa_fwd call = the whole hot path over one batch):
+    B=8, H=32, N=8192, d=128, causal, bf16 inputs iid U(-0.8, 0.8) (seed 1004),
+    the shape of the chipfoundryservices.com "edge/flashattention" model.
+Metric: TFLOP/s with FLOPs = 2*B*H*N^2*d (causal; 4*B*H*N^2*d non-causal).
+
+Prints ONE JSON line.  ``value`` is device-timed with inputs resident in HBM (1.6 GB,
+larger than L2, so no flush between steps); ``e2e`` is the same metric through the
+same C-ABI call with pinned host buffers and the host<->device copies in the timed
+region; ``roofline`` relates the kernel to the measured bf16 tensor peak;
+``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` times that oracle alone as the reference arm.
+Multi-GPU (torchrun): every rank runs its own copy of the workload (weak scaling,
+no data-path collective); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "FA fwd TFLOP/s (causal 2BHN²d) at b8 h32 S8192 d128 bf16; % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+SOURCES = ["tiled_online_softmax_fa_gb300/csrc/fa_api.cu",
+           "tiled_online_softmax_fa_gb300/csrc/fa_fwd_kernel.cuh",
+           "tiled_online_softmax_fa_gb300/csrc/ptx_sm103.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
+
+
+def model_flops(B, H, N, d, causal) -> float:
+    return (2.0 if causal else 4.0) * B * H * N * N * d
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        if pk.get("bf16_tflops"):
+            return float(pk["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
+
+
+# --------------------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.active = False
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rec = {"sm": float(parts[1]), "max": float(parts[2]),
+                       "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                       "hw_slowdown": parts[5], "hw_thermal": parts[6],
+                       "sw_thermal": parts[7], "sw_power_cap": parts[8]}
+            except ValueError:
+                continue
+            rec["in_region"] = self.active
+            self.samples.append(rec)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        region = [s for s in self.samples if s["in_region"]]
+        if not region:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for s in region:
+            for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"),
+                              ("sw_power_cap", "sw_power_cap")):
+                if s[key].lower() == "active":
+                    reasons.add(name)
+        powers = [s["power"] for s in region if s["power"] is not None]
+        return {"sm_mhz": statistics.median(s["sm"] for s in region),
+                "sm_max_mhz": max(s["max"] for s in region),
+                "reasons": sorted(reasons), "samples": len(region),
+                "power_w_max": max(powers) if powers else None}
+
+
+# --------------------------------------------------------------------------------------
+# distributed plumbing (weak scaling: independent copies, max time over ranks)
+# --------------------------------------------------------------------------------------
+def dist_info():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank owns an independent batch of the workload (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline)
+# --------------------------------------------------------------------------------------
+def oracle_rows_flops(rows: np.ndarray, N: int, d: int, causal: bool) -> float:
+    keys = (rows[:, 1] + 1) if causal else np.full(len(rows), N)
+    return float(4.0 * d * keys.sum())
+
+
+def time_oracle(q, k, v, causal, scale, seconds: float, seed: int = 12345):
+    """Run the oracle on seeded random query rows for about `seconds` of wall time.
+
+    Returns (FLOP/s, rows done, seconds spent, threads used)."""
+    import oracle
+    BH = q.shape[0] * q.shape[1]
+    N, d = q.shape[2], q.shape[3]
+    rng = np.random.default_rng(seed)
+    nthreads = oracle.default_threads()
+    done_rows, flops, elapsed = 0, 0.0, 0.0
+    chunk = max(nthreads * 2, 32)
+    while elapsed < seconds:
+        rows = np.stack([rng.integers(0, BH, chunk), rng.integers(0, N, chunk)], axis=1)
+        rows = rows[np.lexsort((rows[:, 1], rows[:, 0]))]
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, rows, causal, scale, nthreads)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        flops += oracle_rows_flops(rows, N, d, causal)
+        done_rows += chunk
+        if dt < seconds / 8:
+            chunk *= 2
+    return flops / elapsed, done_rows, elapsed, nthreads
+
+
+# --------------------------------------------------------------------------------------
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--B", type=int, default=8)
+    ap.add_argument("--H", type=int, default=32)
+    ap.add_argument("--N", type=int, default=8192)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--noncausal", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(--steps, 100)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+def workload_name(args):
+    causal = not args.noncausal
+    if (args.B, args.H, args.N, args.d, causal) == (8, 32, 8192, 128, True):
+        return "b8 h32 S8192 d128 causal (b8n8k)", causal
+    return f"b{args.B} h{args.H} S{args.N} d{args.d} {'causal' if causal else 'non-causal'}", causal
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if world > 1 and rank != 0:
+        return 0
+    w = workloads.WORKLOADS["b8n8k"]
+    name, causal = workload_name(args)
+    q, k, v = workloads.make_inputs(w, B=args.B, H=args.H, N=args.N, d=args.d)
+    scale = float(np.float32(1.0 / np.sqrt(args.d)))
+    # size each step so warm-up + steps take about two minutes of CPU time
+    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    time_oracle(q, k, v, causal, scale, per_step * max(1, args.warmup), seed=1)
+    vals, times, rows_total, threads = [], [], 0, 0
+    for s in range(args.steps):
+        val, rows, el, threads = time_oracle(q, k, v, causal, scale, per_step, seed=100 + s)
+        vals.append(val)
+        times.append(el)
+        rows_total += rows
+    value = float(np.mean(vals)) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "B": args.B, "H": args.H, "N": args.N, "d": args.d,
+                   "causal": causal, "step": "fp64 CPU oracle over a bounded random-row sample"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_total} random query rows over {args.steps} steps "
+                                   f"(~{per_step:.2f} s each) of the {name} workload"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import tiled_online_softmax_fa_gb300 as fa
+
+    world, rank, local = dist_info()
+    if world == 1 and args.gpus > 1:
+        raise SystemExit("--gpus > 1 needs torchrun (one process per GPU)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    fa.load_library()
+    name, causal = workload_name(args)
+    B, H, N, d = args.B, args.H, args.N, args.d
+    w = workloads.WORKLOADS["b8n8k"]
+    q, k, v = workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=shard_seed(w.seed, rank))
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = model_flops(B, H, N, d, causal)
+
+    def step():
+        fa.fa_fwd(qd, kd, vd, o=o, lse=lse, causal=causal, scale=scale, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.get_device_status(stream) != fa.FA_OK:
+        raise SystemExit("device status reported a timeout during warm-up")
+
+    sampler = None if args.no_clocks else ClockSampler(local)
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.active = True
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.active = False
+    barrier(world)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    status = fa.get_device_status(stream)
+    if status != fa.FA_OK:
+        raise SystemExit(f"device status after timing: {fa.strerror(status)}")
+    ms_step = ms_total / args.steps
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    kernel_tflops = flops / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end: pinned host buffers -> H2D -> fa_fwd -> D2H, every step ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        n_e2e = args.e2e_steps or min(args.steps, 100)
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            fa.fa_fwd(qd, kd, vd, o=o, lse=lse, causal=causal, scale=scale, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 3 * q.numel() * 2,
+               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+               "steps": n_e2e, "ms_per_step": ms_e2e}
+        if fa.get_device_status(stream) != fa.FA_OK:
+            raise SystemExit("device status reported a timeout during the e2e leg")
+
+    if sampler:
+        sampler.stop()
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_src = load_peaks()
+    traffic, traffic_note = None, "no ncu capture matching this kernel source"
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_hash") == kernel_source_hash() and \
+                tr.get("shape") == [B, H, N, d, int(causal)]:
+            traffic = tr.get("dram_bytes_per_launch")
+            traffic_note = tr.get("note", "")
+    roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": kernel_tflops / peak, "traffic": traffic, "traffic_note": traffic_note,
+                "peak_source": peak_src, "algorithmic_flops_per_launch": flops,
+                "qkvo_compulsory_bytes_per_launch": 4 * B * H * N * d * 2 + B * H * N * 4,
+                "avg_launch_ms": ms_step, "kernel": f"fa_fwd_kernel<{d}>"}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        val, rows, el, threads = time_oracle(q, k, v, causal, scale, args.cpu_seconds)
+        cpu = {"value": val / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{rows} random query rows of the {name} workload, fp64, {el:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "global_batch": B * world, "seq_len": N, "parallelism": f"replicas{world}",
+                   "l2": "inputs (3 x 537 MB) larger than L2; no flush"},
+        "clocks": sampler.summary() if sampler else None, "e2e": e2e,
+        "gpu_launches": args.steps, "roofline": roofline, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
