@@ -111,6 +111,12 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.nkv = static_cast<int>((N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN);
   p.nqb = static_cast<int>((N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows);
   p.num_units = static_cast<int>(static_cast<int64_t>(p.nqb) * BH);
+  // heads per scheduling group: their K and V together take at most ~64 MB of L2
+  const int64_t kv_bytes_per_head = 2 * N * HD * 2;
+  int64_t g = (int64_t{64} << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  p.group_heads = static_cast<int>(g);
   p.causal = causal ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.budget = (opts && opts->wait_budget_cycles > 0) ? opts->wait_budget_cycles : kDefaultBudget;

@@ -8,8 +8,11 @@
 //
 // GB300 mapping (not from the pages; designed for sm_103a):
 //   * Work unit = one (batch*head, 256-query-row block) = two 128-row Q tiles that
-//     share every K/V tile.  Persistent CTAs (one per SM) walk the units in a static
-//     round-robin over a longest-first order (causal units shrink with the block index).
+//     share every K/V tile.  Persistent CTAs (one per SM) take units in a snake
+//     (boustrophedon) round-robin over this order: heads in groups whose K and V fit
+//     comfortably in L2, and inside a group the longest causal blocks first, so the
+//     units running at one time share a few heads' K/V through L2 and the per-CTA
+//     work evens out.
 //   * Warp roles (384 threads = 3 warpgroups): warps 0-3 = softmax for Q tile 0,
 //     warps 4-7 = softmax for Q tile 1 (one thread per query row), warp 8 = tcgen05
 //     MMA issuer (one lane), warp 9 = TMA producer (one lane), warps 10-11 idle.  The
@@ -81,6 +84,7 @@ struct Params {
   int nkv;            // ceil(N / 128)
   int nqb;            // ceil(N / 256)
   int num_units;      // nqb * BH
+  int group_heads;    // heads whose units are interleaved (K/V of a group fit in L2)
   int causal;
   float scale_log2;   // scale * log2(e), >= 0
   long long budget;   // cycles a single wait may take
@@ -95,10 +99,25 @@ struct Barriers {
   int abort;
 };
 
+// Unit u -> (head, first query row).  Heads are taken in groups of group_heads (the
+// last group may be smaller); inside a group the highest query block of every head
+// comes first, then the next block of every head, and so on.
 __device__ __forceinline__ void unit_coords(int u, const Params& p, int& bh, int& row0) {
-  const int qb = p.nqb - 1 - u / p.BH;  // longest causal units first
-  bh = u % p.BH;
+  const int per_group = p.group_heads * p.nqb;
+  const int g = u / per_group;
+  const int first = g * p.group_heads;
+  const int heads = (p.BH - first) < p.group_heads ? (p.BH - first) : p.group_heads;
+  const int r = u - g * per_group;
+  const int qb = p.nqb - 1 - r / heads;
+  bh = first + r % heads;
   row0 = qb * kUnitRows;
+}
+
+// The k-th unit of this CTA (snake order over the grid); may be >= num_units.
+__device__ __forceinline__ int unit_of(int k) {
+  const int pos = (k & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                          : static_cast<int>(blockIdx.x);
+  return k * static_cast<int>(gridDim.x) + pos;
 }
 
 // Number of K/V tiles a Q tile starting at `row_start` visits (0 if it holds no row < N).
@@ -145,7 +164,9 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
   uint32_t ring = 0;          // K/V ring entries issued so far
   uint32_t units = 0;         // units whose Q was issued
   uint32_t skipped = 0xFFFFFFFFu;
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_units) continue;
     int bh, row0;
     unit_coords(u, p, bh, row0);
     const int n0 = tiles_for(row0, p), n1 = tiles_for(row0 + kBlockM, p);
@@ -221,7 +242,9 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
   const uint32_t q_addr[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE_BYTES)};
   const uint32_t col_s[2] = {kColS0, kColS1}, col_o[2] = {kColO0, kColO1};
   const uint32_t ring_addr = smem_u32(sRing);
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_units) continue;
     int bh, row0;
     unit_coords(u, p, bh, row0);
     const int nt[2] = {tiles_for(row0, p), tiles_for(row0 + kBlockM, p)};
@@ -292,50 +315,53 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// `half` selects columns [64*half, 64*half + 64); the 32 packed words go to pk.
+// `quarter` selects columns [32*quarter, 32*quarter + 32); the 16 packed words go to pk.
+// P = 2^(s*c - m) two columns at a time (packed f32x2 FMA), rounded to bf16x2.
 // Returns {sum of the exact fp32 P, sum of the bf16-rounded P}.
 template <bool MASK>
-__device__ __forceinline__ float2 exp_pack_half(const uint32_t (&s)[128], uint32_t (&pk)[32],
-                                                int half, float c, float neg_m, int lim) {
-  float e0 = 0.f, e1 = 0.f, r0 = 0.f, r1 = 0.f;
+__device__ __forceinline__ float2 exp_pack_quarter(const uint32_t (&s)[128], uint32_t (&pk)[16],
+                                                   int quarter, uint64_t c2, uint64_t negm2,
+                                                   int lim) {
+  uint64_t esum = 0, rsum = 0;  // two fp32 zeros each
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int col = 64 * half + 2 * i;
-    float p0 = ex2_approx(fmaf(__uint_as_float(s[col]), c, neg_m));
-    float p1 = ex2_approx(fmaf(__uint_as_float(s[col + 1]), c, neg_m));
+  for (int i = 0; i < 16; ++i) {
+    const int col = 32 * quarter + 2 * i;
+    const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[col]), __uint_as_float(s[col + 1])), c2,
+                                 negm2);
+    float a0, a1;
+    f32x2_split(x, a0, a1);
+    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
     if (MASK) {
       if (col > lim) p0 = 0.f;
       if (col + 1 > lim) p1 = 0.f;
     }
     const uint32_t w = pack_bf16x2(p0, p1);
     pk[i] = w;
-    e0 += p0;
-    e1 += p1;
-    r0 += __uint_as_float(w << 16);
-    r1 += __uint_as_float(w & 0xFFFF0000u);
+    esum = add_f32x2(esum, f32x2(p0, p1));
+    rsum = add_f32x2(rsum, f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
   }
+  float e0, e1, r0, r1;
+  f32x2_split(esum, e0, e1);
+  f32x2_split(rsum, r0, r1);
   return make_float2(e0 + e1, r0 + r1);
 }
 
 template <bool MASK>
 __device__ __forceinline__ float row_max(const uint32_t (&s)[128], int lim) {
-  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int i = 0; i < 128; i += 4) {
-    float x0 = __uint_as_float(s[i]), x1 = __uint_as_float(s[i + 1]);
-    float x2 = __uint_as_float(s[i + 2]), x3 = __uint_as_float(s[i + 3]);
-    if (MASK) {
-      if (i > lim) x0 = -INFINITY;
-      if (i + 1 > lim) x1 = -INFINITY;
-      if (i + 2 > lim) x2 = -INFINITY;
-      if (i + 3 > lim) x3 = -INFINITY;
+  for (int i = 0; i < 128; i += 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float x0 = __uint_as_float(s[i + 2 * k]), x1 = __uint_as_float(s[i + 2 * k + 1]);
+      if (MASK) {
+        if (i + 2 * k > lim) x0 = -INFINITY;
+        if (i + 2 * k + 1 > lim) x1 = -INFINITY;
+      }
+      m[k] = max3(m[k], x0, x1);
     }
-    m0 = fmaxf(m0, x0);
-    m1 = fmaxf(m1, x1);
-    m2 = fmaxf(m2, x2);
-    m3 = fmaxf(m3, x3);
   }
-  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  return max3(m[0], m[1], fmaxf(m[2], m[3]));
 }
 
 template <int HD>
@@ -347,8 +373,11 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, const Params& p) {
   const uint32_t tS = tmem + lane_base + (t == 0 ? kColS0 : kColS1);
   const uint32_t tO = tmem + lane_base + (t == 0 ? kColO0 : kColO1);
   const float c = p.scale_log2;
+  const uint64_t c2 = f32x2(c, c);
   uint32_t s_cnt = 0, o_cnt = 0;
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_units) continue;
     int bh, row0;
     unit_coords(u, p, bh, row0);
     const int row_start = row0 + t * kBlockM;
@@ -373,36 +402,37 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, const Params& p) {
       const float mx = warp_mask ? row_max<true>(s, lim) : row_max<false>(s, lim);
       const float mt = mx * c;
       const bool need = mt > m_ref + kRescaleLog2;  // also true while m_ref is -inf
-      if (__any_sync(0xFFFFFFFFu, need)) {
-        float alpha = 1.f;
-        if (need) {
-          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
-          m_ref = mt;
-          l_exact *= alpha;
-          l_round *= alpha;
-        }
-        if (j > 0) {
-          // PV_t(j-1) has completed (S_t(j) was issued after it): rescale O_t in place
-#pragma unroll
-          for (int c0 = 0; c0 < HD; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(tO + c0, o);
-            tmem_wait_ld(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_x32(tO + c0, o);
-          }
-        }
+      const bool warp_rescale = __any_sync(0xFFFFFFFFu, need);
+      float alpha = 1.f;
+      if (need) {
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
+        m_ref = mt;
+        l_exact *= alpha;
+        l_round *= alpha;
       }
-      const float neg_m = -m_ref;
+      const uint64_t negm2 = f32x2(-m_ref, -m_ref);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-        const float2 sums = warp_mask ? exp_pack_half<true>(s, pk, half, c, neg_m, lim)
-                                      : exp_pack_half<false>(s, pk, half, c, neg_m, lim);
+      for (int quarter = 0; quarter < 4; ++quarter) {
+        uint32_t pk[16];
+        const float2 sums = warp_mask ? exp_pack_quarter<true>(s, pk, quarter, c2, negm2, lim)
+                                      : exp_pack_quarter<false>(s, pk, quarter, c2, negm2, lim);
         l_exact += sums.x;
         l_round += sums.y;
-        tmem_st_x32(tS + 32 * half, pk);
+        tmem_st_x16(tS + 16 * quarter, pk);
+      }
+      if (warp_rescale && j > 0) {
+        // PV_t(j-1) has completed (S_t(j) was issued after it) and PV_t(j) waits for
+        // this warp's arrival below: rescale O_t in place.  Done after the S row is
+        // consumed so the two never occupy registers together.
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_x32(tO + c0, o);
+        }
       }
       tmem_wait_st();
       tc_fence_before_sync();
