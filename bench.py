@@ -216,6 +216,8 @@ def parse_args(argv=None):
     ap.add_argument("--noncausal", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(--steps, 100)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="CPU time budget of the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -237,8 +239,8 @@ def run_reference(args):
     name, causal = workload_name(args)
     q, k, v = workloads.make_inputs(w, B=args.B, H=args.H, N=args.N, d=args.d)
     scale = float(np.float32(1.0 / np.sqrt(args.d)))
-    # size each step so warm-up + steps take about two minutes of CPU time
-    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    # size each step so warm-up + steps take about --ref-seconds of CPU time
+    per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
     time_oracle(q, k, v, causal, scale, per_step * max(1, args.warmup), seed=1)
     vals, times, rows_total, threads = [], [], 0, 0
     for s in range(args.steps):
