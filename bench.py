@@ -50,6 +50,20 @@ def model_flops(B, H, N, d, causal) -> float:
     return (2.0 if causal else 4.0) * B * H * N * N * d
 
 
+def page_traffic_models(B, H, N, d, elem_bytes=2, block_q=128) -> dict:
+    """HBM bytes of one attention forward as the aiml.sh lab.py page counts them
+    (`estimate_hbm_bytes`), for B batches: Q,K,V read and O written once; the
+    materialised path adding S and P written and read (4 H N^2 elements); causal
+    query-block tiling with no reuse between blocks reading min(N, start + block_q)
+    key and value rows per block."""
+    qkvo = 4 * H * N * d * elem_bytes
+    nxn = 4 * H * N * N * elem_bytes
+    kv_rows = sum(min(N, s + block_q) for s in range(0, N, block_q))
+    tiled = (2 * H * N * d + 2 * H * kv_rows * d) * elem_bytes
+    return {"qkvo_bytes": B * qkvo, "materialised_bytes": B * (qkvo + nxn),
+            "tiled_no_reuse_bytes": B * tiled}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in SOURCES:
@@ -215,12 +229,18 @@ def parse_args(argv=None):
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--noncausal", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(--steps, 100)")
+    ap.add_argument("--e2e-chunks", type=int, default=4, help="batch chunks pipelined per e2e step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="CPU time budget of the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sweep", default="", help="write a sequence-length sweep (JSON) to this path "
+                    "instead of the contract line")
+    ap.add_argument("--sweep-n", default="512,1024,2048,4096,8192,16384,32768,65536,131072")
+    ap.add_argument("--sweep-launches", type=int, default=20, help="timed launches per length "
+                    "(1 = a single untimed launch per length, for an ncu capture)")
     return ap.parse_args(argv)
 
 
@@ -321,39 +341,74 @@ def run_ours(args):
     kernel_tflops = flops / (ms_step * 1e-3) / 1e12
 
     # ---- end to end: pinned host buffers -> H2D -> fa_fwd -> D2H, every step ----
+    # Each step moves its q, k, v in and its o, lse out.  The batch is cut into chunks
+    # on three streams (copy in, compute, copy out) so copies of one chunk overlap the
+    # kernel on another; a chunk's buffers are reused only after the previous step's
+    # kernel (for inputs) and copy-out (for outputs) of that chunk finished.
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.pin_memory() for t in (q, k, v))
         ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
         hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
         n_e2e = args.e2e_steps or min(args.steps, 100)
+        chunks = max(1, min(args.e2e_chunks, B))
+        bounds = [(B * c // chunks, B * (c + 1) // chunks) for c in range(chunks)]
+        s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_done = [ev() for _ in bounds]
+        comp_done = [ev() for _ in bounds]
+        out_done = [ev() for _ in bounds]
+        first = [True]
 
         def e2e_step():
-            qd.copy_(hq, non_blocking=True)
-            kd.copy_(hk, non_blocking=True)
-            vd.copy_(hv, non_blocking=True)
-            fa.fa_fwd(qd, kd, vd, o=o, lse=lse, causal=causal, scale=scale, stream=stream)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+            for c, (b0, b1) in enumerate(bounds):
+                with torch.cuda.stream(s_in):
+                    if not first[0]:
+                        s_in.wait_event(comp_done[c])      # inputs of chunk c are free
+                    qd[b0:b1].copy_(hq[b0:b1], non_blocking=True)
+                    kd[b0:b1].copy_(hk[b0:b1], non_blocking=True)
+                    vd[b0:b1].copy_(hv[b0:b1], non_blocking=True)
+                    in_done[c].record(s_in)
+                s_comp.wait_event(in_done[c])
+                if not first[0]:
+                    s_comp.wait_event(out_done[c])         # outputs of chunk c were read
+                fa.fa_fwd(qd[b0:b1], kd[b0:b1], vd[b0:b1], o=o[b0:b1], lse=lse[b0:b1],
+                          causal=causal, scale=scale, stream=s_comp)
+                comp_done[c].record(s_comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(comp_done[c])
+                    ho[b0:b1].copy_(o[b0:b1], non_blocking=True)
+                    hl[b0:b1].copy_(lse[b0:b1], non_blocking=True)
+                    out_done[c].record(s_out)
+            first[0] = False
 
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize(dev)
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(s_in)
+        s_comp.wait_event(e0)
+        s_out.wait_event(e0)
         for _ in range(n_e2e):
             e2e_step()
-        e1.record(stream)
+        s_in.wait_stream(s_comp)
+        s_in.wait_stream(s_out)
+        e1.record(s_in)
         torch.cuda.synchronize(dev)
         barrier(world)
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
         e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": 3 * q.numel() * 2,
                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
-               "steps": n_e2e, "ms_per_step": ms_e2e}
+               "steps": n_e2e, "ms_per_step": ms_e2e, "chunks_per_step": chunks,
+               "launches_per_step": chunks}
         if fa.get_device_status(stream) != fa.FA_OK:
             raise SystemExit("device status reported a timeout during the e2e leg")
+        # the pipelined copies must return exactly what the device computed
+        torch.cuda.synchronize(dev)
+        if not (torch.equal(ho, o.cpu()) and torch.equal(hl, lse.cpu())):
+            raise SystemExit("e2e outputs differ from the device outputs")
 
     if sampler:
         sampler.stop()
@@ -399,8 +454,58 @@ def run_ours(args):
     return 0
 
 
+def run_sweep(args):
+    """Measured TFLOP/s per sequence length beside the pages' traffic models."""
+    import tiled_online_softmax_fa_gb300 as fa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    causal = not args.noncausal
+    B, H, d = args.B, args.H, args.d
+    w = workloads.WORKLOADS["b8n8k"]
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    stream = torch.cuda.current_stream(dev)
+    results = []
+    for N in [int(x) for x in args.sweep_n.split(",")]:
+        q, k, v = (t.to(dev) for t in workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=7000 + N))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale, stream=stream)  # noqa: E731
+        rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal,
+               "flops": model_flops(B, H, N, d, causal)}
+        if args.sweep_launches <= 1:
+            run()
+            torch.cuda.synchronize(dev)
+        else:
+            for _ in range(3):
+                run()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.sweep_launches):
+                run()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / args.sweep_launches
+            rec.update(ms=ms, tflops=rec["flops"] / (ms * 1e-3) / 1e12)
+        if fa.get_device_status(stream) != fa.FA_OK:
+            raise SystemExit(f"device status reported a timeout at N={N}")
+        rec.update(page_traffic_models(B, H, N, d), lse_bytes=B * H * N * 4)
+        results.append(rec)
+        print(json.dumps(rec), flush=True)
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+    peak, peak_src = load_peaks()
+    with open(args.sweep, "w") as f:
+        json.dump({"peak_tflops": peak, "peak_source": peak_src, "results": results}, f, indent=1)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -72,3 +72,14 @@ def test_reference_arm_json_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["higher_is_better"] is True and line["metric"] == bench.METRIC
+
+
+def test_page_traffic_models_match_the_page():
+    """bench.py's statement of the page's traffic model reproduces the printed sweep."""
+    with open(os.path.join(ROOT, "tests", "golden", "page_hbm_traffic_sweep.json")) as f:
+        rows = json.load(f)["rows"]
+    for r in rows:
+        m = bench.page_traffic_models(1, r["num_heads"], r["seq_len"], r["head_dim"])
+        assert round(m["qkvo_bytes"] / 1e6, 2) == r["qkvo_compulsory_bytes_mb"]
+        assert round(m["materialised_bytes"] / 1e6, 2) == r["standard_total_hbm_mb"]
+        assert round(m["tiled_no_reuse_bytes"] / 1e6, 2) == r["tiled_logical_access_mb_no_cache_reuse"]
