@@ -42,7 +42,8 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 SOURCES = ["tiled_online_softmax_fa_gb300/csrc/fa_api.cu",
            "tiled_online_softmax_fa_gb300/csrc/fa_fwd_kernel.cuh",
-           "tiled_online_softmax_fa_gb300/csrc/ptx_sm103.cuh"]
+           "tiled_online_softmax_fa_gb300/csrc/ptx_sm103.cuh",
+           "tiled_online_softmax_fa_gb300/csrc/fa_merge_kernel.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
 
 
@@ -239,6 +240,8 @@ def parse_args(argv=None):
     ap.add_argument("--sweep", default="", help="write a sequence-length sweep (JSON) to this path "
                     "instead of the contract line")
     ap.add_argument("--sweep-n", default="512,1024,2048,4096,8192,16384,32768,65536,131072")
+    ap.add_argument("--splits", type=int, default=1, help="sweep: key-range splits (0 = auto, "
+                    "1 = the unsplit kernel)")
     ap.add_argument("--sweep-launches", type=int, default=20, help="timed launches per length "
                     "(1 = a single untimed launch per length, for an ncu capture)")
     return ap.parse_args(argv)
@@ -471,8 +474,15 @@ def run_sweep(args):
         q, k, v = (t.to(dev) for t in workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=7000 + N))
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale, stream=stream)  # noqa: E731
-        rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal,
+        splits = args.splits if args.splits > 0 else fa.splitkv_auto_splits(B, H, N, causal)
+        if splits > 1:
+            ws = torch.empty(fa.splitkv_workspace_bytes(B, H, N, d, splits), dtype=torch.uint8,
+                             device=dev)
+            run = lambda: fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, causal=causal, scale=scale,  # noqa: E731
+                                            splits=splits, workspace=ws, stream=stream)
+        else:
+            run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale, stream=stream)  # noqa: E731
+        rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal, "splits": splits,
                "flops": model_flops(B, H, N, d, causal)}
         if args.sweep_launches <= 1:
             run()

@@ -21,6 +21,7 @@
 #ifndef FA_SM103_H
 #define FA_SM103_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -84,6 +85,38 @@ typedef struct {
 int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse,
                 int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
                 void* stream, const fa_fwd_options* opts);
+
+/*
+ * Split-KV forward (the same result as fa_fwd, more parallelism for small B*H*N).
+ *
+ * Each 256-row query block's key range is cut into `splits` pieces processed by
+ * different CTAs; every piece writes its normalised partial output O_s and the
+ * logsumexp lse_s of its scores to `workspace`, and a second kernel merges them:
+ *     lse = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s.
+ * The pages do not describe this; it follows from the definition above (the
+ * logsumexp of a union of key ranges), and it is what the lse output enables.
+ *
+ *   splits     1..64, or 0 to let the library choose (fa_splitkv_auto_splits);
+ *              1 runs fa_fwd and needs no workspace.
+ *   workspace  device memory, 16-byte aligned, caller-owned, at least
+ *              fa_splitkv_workspace_bytes(B, H, N, d, splits) bytes (use the count from
+ *              fa_splitkv_auto_splits for splits = 0); must not overlap any tensor.
+ *              Its contents on entry do not matter; they are scratch after the call.
+ * Other arguments, ownership and errors as fa_fwd.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                   int splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_splitkv needs for these sizes and `splits` (>= 1); -1 on bad arguments. */
+int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits);
+
+/*
+ * The split count fa_fwd_splitkv uses for splits = 0 on the current device (1 on error):
+ * more than one only when the longest query block's key range would be the critical
+ * path (few, long blocks for the number of SMs, e.g. one head at N = 32768).
+ */
+int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
 
 /* Static description of a status code. Never NULL. */
 const char* fa_strerror(int status);

@@ -31,7 +31,8 @@ def test_library_builds_and_loads():
 def test_every_declared_symbol_is_exported():
     names = _declared_functions()
     assert {"fa_fwd", "fa_fwd_opts", "fa_strerror", "fa_last_error", "fa_get_device_status",
-            "fa_version"} <= set(names)
+            "fa_version", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes",
+            "fa_splitkv_auto_splits"} <= set(names)
     lib = fa.load_library()
     for name in names:
         assert hasattr(lib, name), name
@@ -89,3 +90,34 @@ def test_python_wrapper_rejects_cpu_tensors():
     t = torch.zeros((1, 1, 8, 16), dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         fa.fa_fwd(t, t, t)
+
+
+def test_splitkv_workspace_bytes():
+    # 256-row units, per item 256 rows of (d fp32 partial O + 1 fp32 lse)
+    units = 1 * 32 * (1024 // 256)
+    assert fa.splitkv_workspace_bytes(1, 32, 1024, 128, 4) == units * 4 * 256 * (128 + 1) * 4
+    assert fa.splitkv_workspace_bytes(1, 32, 1024, 128, 1) == 0
+    assert fa.splitkv_workspace_bytes(1, 32, 1024, 48, 4) == -1
+    assert fa.splitkv_workspace_bytes(1, 32, 1024, 128, 0) == -1
+    assert fa.splitkv_workspace_bytes(0, 32, 1024, 128, 4) == 0
+
+
+def _split(**kw):
+    args = dict(q_ptr=0x10000, k_ptr=0x20000, v_ptr=0x30000, o_ptr=0x40000, lse_ptr=0, B=1, H=1,
+                N=128, d=64, causal=True, scale=0.1, splits=3, ws_ptr=0x100000, ws_bytes=10 ** 9)
+    args.update(kw)
+    return fa.fa_fwd_splitkv_raw(**args)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ws_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=100), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_ptr=0x100008), fa.FA_ERR_MISALIGNED),
+    (dict(splits=65), fa.FA_ERR_INVALID_ARG),
+    (dict(splits=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_ptr=0x20000), fa.FA_ERR_INVALID_ARG),      # workspace overlaps k
+    (dict(d=40), fa.FA_ERR_UNSUPPORTED),
+])
+def test_splitkv_argument_errors(kw, want):
+    assert _split(**kw) == want
+    assert fa.last_error() != ""

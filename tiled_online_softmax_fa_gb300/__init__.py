@@ -13,7 +13,8 @@ import threading
 
 from . import build as _build
 
-__all__ = ["fa_fwd", "fa_fwd_raw", "get_device_status", "strerror", "last_error", "version",
+__all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_splitkv", "fa_fwd_splitkv_raw",
+           "splitkv_workspace_bytes", "splitkv_auto_splits", "get_device_status", "strerror", "last_error", "version",
            "load_library", "FAError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED",
            "FA_ERR_MISALIGNED", "FA_ERR_ARCH", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
            "FwdOptions", "SUPPORTED_HEAD_DIMS"]
@@ -69,6 +70,13 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.fa_get_device_status.restype = ctypes.c_int
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ctypes.c_int
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv.restype = ctypes.c_int
+        lib.fa_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.c_int]
+        lib.fa_splitkv_workspace_bytes.restype = ctypes.c_int64
+        lib.fa_splitkv_auto_splits.argtypes = [i64, i64, i64, ctypes.c_int]
+        lib.fa_splitkv_auto_splits.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -138,6 +146,57 @@ def fa_fwd(q, k, v, o=None, lse=None, causal: bool = True, scale: float | None =
                     _stream_handle(stream, q.device), options)
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
+    return o, lse
+
+
+def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, splits: int) -> int:
+    return int(load_library().fa_splitkv_workspace_bytes(B, H, N, d, splits))
+
+
+def splitkv_auto_splits(B: int, H: int, N: int, causal: bool = True) -> int:
+    return int(load_library().fa_splitkv_auto_splits(B, H, N, int(bool(causal))))
+
+
+def fa_fwd_splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal, scale, splits,
+                       ws_ptr, ws_bytes, stream: int = 0) -> int:
+    """Call fa_fwd_splitkv with raw device addresses; returns the status code."""
+    lib = load_library()
+    return int(lib.fa_fwd_splitkv(q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None,
+                                  lse_ptr or None, int(B), int(H), int(N), int(d),
+                                  int(bool(causal)), float(scale), int(splits), ws_ptr or None,
+                                  int(ws_bytes), stream or None))
+
+
+def fa_fwd_splitkv(q, k, v, o=None, lse=None, causal: bool = True, scale: float | None = None,
+                   splits: int = 0, workspace=None, stream=None):
+    """fa_fwd with each query block's key range split across CTAs and merged by lse.
+
+    splits = 0 lets the library choose.  ``workspace`` (a CUDA uint8 tensor) is
+    allocated here when not given.  Returns (o, lse).
+    """
+    import torch
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    use = splits if splits > 0 else splitkv_auto_splits(B, H, N, causal)
+    need = splitkv_workspace_bytes(B, H, N, d, use) if use > 1 else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 \
+                or not t.is_contiguous() or t.shape != q.shape:
+            raise TypeError(f"{name} must be a contiguous CUDA bf16 tensor shaped like q")
+    rc = fa_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), B, H, N, d, causal, scale, use, ws_ptr, ws_bytes,
+                            _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_splitkv")
     return o, lse
 
 

@@ -12,6 +12,7 @@
 
 #include "../../include/fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_merge_kernel.cuh"
 
 namespace {
 
@@ -86,10 +87,65 @@ int encode_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_
   return FA_OK;
 }
 
+constexpr int kMaxSplits = 64;
+
+int64_t units_for(int64_t BH, int64_t N) {
+  return ((N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows) * BH;
+}
+
+// Bytes of workspace a split launch needs: per item 256 rows of normalised partial O
+// (fp32, d per row) and 256 partial logsumexps.
+int64_t workspace_bytes(int64_t BH, int64_t N, int64_t d, int splits) {
+  if (splits <= 1) return 0;
+  const int64_t rows = units_for(BH, N) * splits * fa_sm103::kUnitRows;
+  return rows * d * 4 + rows * 4;
+}
+
+// Split only when the longest unit would be the critical path -- its key tiles exceed
+// twice the average work per SM -- and that average is large enough (>= 16 tiles) to
+// amortise a piece's fixed costs and the merge.  Pieces are ~1.5x the average.
+// (Measured on GB300, B1 d128 causal: H1 N32768 548 -> 946 TFLOP/s and H4 N8192
+// 515 -> 644 TFLOP/s with two pieces; H8 N4096 and B1 H32 N2048 are faster unsplit.)
+int choose_splits(int64_t BH, int64_t N, int num_sms, int causal) {
+  const int64_t nqb = (N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows;
+  const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
+  const int64_t n_max = causal ? (2 * nqb < nkv ? 2 * nqb : nkv) : nkv;
+  // key tiles over all units (a unit does max(n0, n1) tile steps)
+  int64_t total = 0;
+  for (int64_t qb = 0; qb < nqb; ++qb) total += causal ? (2 * qb + 2 < nkv ? 2 * qb + 2 : nkv) : nkv;
+  total *= BH;
+  const double per_sm = static_cast<double>(total) / num_sms;
+  if (n_max <= 2.0 * per_sm || per_sm < 16.0) return 1;
+  int64_t sp = static_cast<int64_t>(std::ceil(static_cast<double>(n_max) / (1.5 * per_sm)));
+  if (sp > kMaxSplits) sp = kMaxSplits;
+  return sp < 1 ? 1 : static_cast<int>(sp);
+}
+
+// Workspace large enough for `splits` and clear of every tensor (sets the error text).
+bool workspace_fits(const void* ws, size_t size, int64_t BH, int64_t N, int64_t d, int splits,
+                    const void* q, const void* k, const void* v, const void* o, size_t bytes,
+                    const void* lse, size_t lse_bytes) {
+  const int64_t need = workspace_bytes(BH, N, d, splits);
+  if (static_cast<int64_t>(size) < need) {
+    set_error(FA_ERR_INVALID_ARG, "workspace too small (see fa_splitkv_workspace_bytes)");
+    return false;
+  }
+  for (const void* t : {q, k, v, o})
+    if (overlaps(ws, static_cast<size_t>(need), t, bytes)) {
+      set_error(FA_ERR_INVALID_ARG, "workspace overlaps a tensor");
+      return false;
+    }
+  if (lse && overlaps(ws, static_cast<size_t>(need), lse, lse_bytes)) {
+    set_error(FA_ERR_INVALID_ARG, "workspace overlaps lse");
+    return false;
+  }
+  return true;
+}
+
 template <int HD>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
            int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
-           bool& smem_set, const fa_fwd_options* opts) {
+           bool& smem_set, const fa_fwd_options* opts, int splits, void* workspace) {
   using C = fa_sm103::Cfg<HD>;
   CUtensorMap mq, mk, mv;
   int st;
@@ -111,6 +167,12 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.nkv = static_cast<int>((N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN);
   p.nqb = static_cast<int>((N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows);
   p.num_units = static_cast<int>(static_cast<int64_t>(p.nqb) * BH);
+  p.splits = splits;
+  p.num_items = p.num_units * splits;
+  p.ws_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.ws_lse = splits > 1 ? static_cast<float*>(workspace) +
+                              static_cast<size_t>(p.num_items) * fa_sm103::kUnitRows * HD
+                        : nullptr;
   // heads per scheduling group: their K and V together take at most ~64 MB of L2
   const int64_t kv_bytes_per_head = 2 * N * HD * 2;
   int64_t g = (int64_t{64} << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
@@ -123,10 +185,18 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.inject = opts ? opts->inject_skip_kv_load : 0;
   int grid = dev.num_sms;
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
-  if (grid > p.num_units) grid = p.num_units;
+  if (grid > p.num_items) grid = p.num_items;
   fa_sm103::fa_fwd_kernel<HD><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
+  if (splits > 1) {
+    const int64_t warps = BH * N;
+    const int64_t blocks = (warps + fa_sm103::kMergeThreads / 32 - 1) / (fa_sm103::kMergeThreads / 32);
+    fa_sm103::fa_merge_kernel<HD><<<static_cast<unsigned>(blocks), fa_sm103::kMergeThreads, 0,
+                                    stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
+  }
   return FA_OK;
 }
 
@@ -165,9 +235,15 @@ int device_state(DeviceState** out) {
 
 extern "C" {
 
-int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
-                int64_t H, int64_t N, int64_t d, int causal, float scale, void* stream,
-                const fa_fwd_options* opts) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of every forward entry point.  splits = 0 chooses a split count (only
+// used when workspace is non-null); splits = 1 is the unsplit kernel.
+int forward(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+            int64_t H, int64_t N, int64_t d, int causal, float scale, void* stream,
+            const fa_fwd_options* opts, int splits, void* workspace, size_t workspace_size) {
   t_last_error.clear();
   // ---- pure argument checks: no CUDA call before these pass ----
   if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
@@ -198,20 +274,67 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
   if (lse && overlaps(lse, lse_bytes, o, bytes)) return set_error(FA_ERR_INVALID_ARG, "lse overlaps o");
   if (opts && (opts->wait_budget_cycles < 0 || opts->inject_skip_kv_load < 0 || opts->max_ctas < 0))
     return set_error(FA_ERR_INVALID_ARG, "negative option");
+  if (splits < 0 || splits > kMaxSplits)
+    return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
+  if (splits > 1 || (splits == 0 && workspace)) {
+    if (!workspace) return set_error(FA_ERR_INVALID_ARG, "a split launch needs a workspace");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+      return set_error(FA_ERR_MISALIGNED, "workspace not 16-byte aligned");
+  }
+  if (splits > 1 && !workspace_fits(workspace, workspace_size, BH, N, d, splits, q, k, v, o,
+                                    bytes, lse, lse_bytes))
+    return FA_ERR_INVALID_ARG;
 
   // ---- device checks ----
   DeviceState* dev = nullptr;
   int st = device_state(&dev);
   if (st != FA_OK) return st;
   if (!dev->arch_ok) return set_error(FA_ERR_ARCH, "device is not sm_103 (GB300-class)");
+  if (splits == 0) {
+    splits = choose_splits(BH, N, dev->num_sms, causal);
+    if (splits > 1 && !workspace_fits(workspace, workspace_size, BH, N, d, splits, q, k, v, o,
+                                      bytes, lse, lse_bytes))
+      return FA_ERR_INVALID_ARG;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool& smem_set = dev->smem_set[hd];
   switch (hd) {
-    case 0: return launch<16>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
-    case 1: return launch<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
-    case 2: return launch<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
-    default: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
+    case 0: return launch<16>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    case 1: return launch<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    case 2: return launch<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    default: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
   }
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                int64_t H, int64_t N, int64_t d, int causal, float scale, void* stream,
+                const fa_fwd_options* opts) {
+  return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, opts, 1, nullptr, 0);
+}
+
+int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits) {
+  if (B < 0 || H < 0 || N < 0 || head_dim_index(d) < 0 || splits < 1 || splits > kMaxSplits)
+    return -1;
+  if (B == 0 || H == 0 || N == 0) return 0;
+  return workspace_bytes(B * H, N, d, splits);
+}
+
+int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal) {
+  if (B <= 0 || H <= 0 || N <= 0) return 1;
+  DeviceState* dev = nullptr;
+  if (device_state(&dev) != FA_OK) return 1;
+  return choose_splits(B * H, N, dev->num_sms, causal);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                   int64_t H, int64_t N, int64_t d, int causal, float scale, int splits,
+                   void* workspace, size_t workspace_bytes_given, void* stream) {
+  return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, nullptr, splits, workspace,
+                 workspace_bytes_given);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,

@@ -85,7 +85,11 @@ struct Params {
   int nkv;            // ceil(N / 128)
   int nqb;            // ceil(N / 256)
   int num_units;      // nqb * BH
+  int splits;         // KV ranges per unit (1 = no split)
+  int num_items;      // num_units * splits
   int group_heads;    // heads whose units are interleaved (K/V of a group fit in L2)
+  float* ws_o;        // splits > 1: per item, normalised partial O [256 rows][HD] (fp32)
+  float* ws_lse;      // splits > 1: per item, partial logsumexp [256 rows]
   int causal;
   float scale_log2;   // scale * log2(e), >= 0
   long long budget;   // cycles a single wait may take
@@ -130,6 +134,24 @@ __device__ __forceinline__ int tiles_for(int row_start, const Params& p) {
   return t < p.nkv ? t : p.nkv;
 }
 
+// A work item: one unit's KV tiles [k0, k1).  Q tile t visits [k0, e[t]), which is
+// empty when e[t] <= k0.  With splits = 1 an item is the whole unit.
+struct Item {
+  int bh, row0, k0, k1;
+  int e[2];
+};
+
+__device__ __forceinline__ void item_coords(int w, const Params& p, Item& it) {
+  const int u = w / p.splits, sp = w - u * p.splits;
+  unit_coords(u, p, it.bh, it.row0);
+  const int n0 = tiles_for(it.row0, p), n1 = tiles_for(it.row0 + kBlockM, p);
+  const int n = n0 > n1 ? n0 : n1;
+  it.k0 = sp * n / p.splits;
+  it.k1 = (sp + 1) * n / p.splits;
+  it.e[0] = n0 < it.k1 ? n0 : it.k1;
+  it.e[1] = n1 < it.k1 ? n1 : it.k1;
+}
+
 __device__ __forceinline__ void raise_abort(Barriers& b) {
   *reinterpret_cast<volatile int*>(&b.abort) = 1;
   atomicOr(&g_device_status, 1u);
@@ -166,14 +188,14 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
   uint32_t ring = 0;          // K/V ring entries issued so far
   uint32_t units = 0;         // units whose Q was issued
   uint32_t skipped = 0xFFFFFFFFu;
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
     const int u = unit_of(k);
-    if (u >= p.num_units) continue;
-    int bh, row0;
-    unit_coords(u, p, bh, row0);
-    const int n0 = tiles_for(row0, p), n1 = tiles_for(row0 + kBlockM, p);
-    const int n = n0 > n1 ? n0 : n1;
-    // Q smem is free once the previous unit's last S MMA has completed
+    if (u >= p.num_items) continue;
+    Item it;
+    item_coords(u, p, it);
+    if (it.k1 <= it.k0) continue;  // an empty KV range (more splits than tiles)
+    const int bh = it.bh, row0 = it.row0;
+    // Q smem is free once the previous item's last S MMA has completed
     if (units > 0 && !wait_bar(&b.q_empty, (units - 1) & 1, p, b)) goto fail;
     mbar_arrive_expect_tx(&b.q_full, 2 * C::TILE_BYTES);
     for (int t = 0; t < 2; ++t)
@@ -181,7 +203,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
         tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, tmQ, &b.q_full, c * C::W,
                     row0 + t * kBlockM, bh);
     ++units;
-    for (int j = 0; j < n; ++j) {
+    for (int j = it.k0; j < it.k1; ++j) {
       for (int kv = 0; kv < 2; ++kv) {
         const uint32_t slot = ring % C::NSLOT, round = ring / C::NSLOT;
         if (round > 0 && !wait_bar(&b.slot_empty[slot], (round - 1) & 1, p, b)) goto fail;
@@ -244,13 +266,13 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
   const uint32_t q_addr[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE_BYTES)};
   const uint32_t col_s[2] = {kColS0, kColS1}, col_o[2] = {kColO0, kColO1};
   const uint32_t ring_addr = smem_u32(sRing);
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
     const int u = unit_of(k);
-    if (u >= p.num_units) continue;
-    int bh, row0;
-    unit_coords(u, p, bh, row0);
-    const int nt[2] = {tiles_for(row0, p), tiles_for(row0 + kBlockM, p)};
-    const int n = nt[0] > nt[1] ? nt[0] : nt[1];
+    if (u >= p.num_items) continue;
+    Item it;
+    item_coords(u, p, it);
+    if (it.k1 <= it.k0) continue;
+    const int k0 = it.k0, k1 = it.k1;
     if (!wait_bar(&b.q_full, units & 1, p, b)) goto fail;
     ++units;
     uint32_t ks = ring % C::NSLOT;
@@ -258,17 +280,17 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
     ++ring;
     tc_fence_after_sync();
     for (int t = 0; t < 2; ++t)
-      if (nt[t] > 0) {
+      if (it.e[t] > k0) {
         issue_s<HD>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::TILE_BYTES);
         mma_commit(&b.s_full[t]);
       }
     mma_commit(&b.slot_empty[ks]);
-    if (n == 1) mma_commit(&b.q_empty);
-    for (int j = 0; j < n; ++j) {
+    if (k1 - k0 == 1) mma_commit(&b.q_empty);
+    for (int j = k0; j < k1; ++j) {
       const uint32_t vs = ring % C::NSLOT;
       if (!wait_bar(&b.slot_full[vs], (ring / C::NSLOT) & 1, p, b)) goto fail;
       ++ring;
-      const bool next = j + 1 < n;
+      const bool next = j + 1 < k1;
       if (next) {
         ks = ring % C::NSLOT;
         if (!wait_bar(&b.slot_full[ks], (ring / C::NSLOT) & 1, p, b)) goto fail;
@@ -276,18 +298,18 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
       }
       tc_fence_after_sync();
       for (int t = 0; t < 2; ++t) {
-        if (j < nt[t]) {
-          if (j == 0) {  // O_t must have been read out by the previous unit's epilogue
+        if (j < it.e[t]) {
+          if (j == k0) {  // O_t must have been read out by the previous item's epilogue
             if (!wait_bar(&b.o_empty[t], (oe_cnt[t] & 1) ^ 1, p, b)) goto fail;
             ++oe_cnt[t];
           }
           if (!wait_bar(&b.p_full[t], p_cnt[t] & 1, p, b)) goto fail;
           ++p_cnt[t];
           tc_fence_after_sync();
-          issue_pv<HD>(tmem + col_o[t], tmem + col_s[t], ring_addr + vs * C::TILE_BYTES, j > 0);
-          if (j == nt[t] - 1) mma_commit(&b.o_full[t]);
+          issue_pv<HD>(tmem + col_o[t], tmem + col_s[t], ring_addr + vs * C::TILE_BYTES, j > k0);
+          if (j == it.e[t] - 1) mma_commit(&b.o_full[t]);
         }
-        if (next && j + 1 < nt[t]) {
+        if (next && j + 1 < it.e[t]) {
           issue_s<HD>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::TILE_BYTES);
           mma_commit(&b.s_full[t]);
         }
@@ -295,7 +317,7 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
       mma_commit(&b.slot_empty[vs]);
       if (next) {
         mma_commit(&b.slot_empty[ks]);
-        if (j + 1 == n - 1) mma_commit(&b.q_empty);
+        if (j + 1 == k1 - 1) mma_commit(&b.q_empty);
       }
     }
   }
@@ -389,20 +411,20 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& 
   const float c = p.scale_log2;
   const uint64_t c2 = f32x2(c, c);
   uint32_t s_cnt = 0, o_cnt = 0, x_cnt = 0;
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
     const int u = unit_of(k);
-    if (u >= p.num_units) continue;
-    int bh, row0;
-    unit_coords(u, p, bh, row0);
+    if (u >= p.num_items) continue;
+    Item it;
+    item_coords(u, p, it);
+    if (it.e[t] <= it.k0) continue;  // this Q tile has no key tile in the item
+    const int bh = it.bh, row0 = it.row0;
     const int row_start = row0 + t * kBlockM;
-    const int nt = tiles_for(row_start, p);
-    if (nt == 0) continue;
     const int row = row_start + lrow;
     // admissible keys for this row: j <= last_key
     const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
     float m_ref = -INFINITY;  // reference maximum, log2 units (identical in both halves)
     float l_exact = 0.f, l_round = 0.f;  // this half's partial sums
-    for (int j = 0; j < nt; ++j) {
+    for (int j = it.k0; j < it.e[t]; ++j) {
       if (!warp_wait(&b.s_full[t], s_cnt & 1, p, b)) goto fail;
       tc_fence_after_sync();
       uint32_t s[64];
@@ -439,7 +461,7 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& 
         l_round += sums.y;
         tmem_st_x16(tP + 16 * part, pk);
       }
-      if (warp_rescale && j > 0) {
+      if (warp_rescale && j > it.k0) {
         // PV_t(j-1) has completed (S_t(j) was issued after it) and PV_t(j) waits for
         // this thread's arrival below: rescale this half's O chunks in place.
 #pragma unroll
@@ -467,7 +489,28 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& 
     if (!warp_wait(&b.o_full[t], o_cnt & 1, p, b)) goto fail;
     ++o_cnt;
     tc_fence_after_sync();
-    {
+    if (p.splits > 1) {
+      // partial result of this KV range: normalised O (fp32) and its logsumexp
+      const float inv_l = 1.f / l_round;
+      const bool store = row < p.N;
+      const size_t slot = static_cast<size_t>(u) * kUnitRows + t * kBlockM + lrow;
+      float* orow = p.ws_o + slot * HD;
+#pragma unroll
+      for (int c0 = 32 * h; c0 < HD; c0 += 64) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + c0, o);
+        tmem_wait_ld(o);
+        if (store) {
+          constexpr int NV = HD < 32 ? HD : 32;
+#pragma unroll
+          for (int v4 = 0; v4 < NV; v4 += 4)
+            *reinterpret_cast<float4*>(orow + c0 + v4) =
+                make_float4(__uint_as_float(o[v4]) * inv_l, __uint_as_float(o[v4 + 1]) * inv_l,
+                            __uint_as_float(o[v4 + 2]) * inv_l, __uint_as_float(o[v4 + 3]) * inv_l);
+        }
+      }
+      if (h == 0 && store) p.ws_lse[slot] = (m_ref + lg2_approx(l_exact)) * kLn2;
+    } else {
       const float inv_l = 1.f / l_round;
       const bool store = row < p.N;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + row) * HD;
