@@ -118,6 +118,35 @@ int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, i
  */
 int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
 
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that may not allocate device
+ * memory.  The source pages have no counterpart; this is a deployment convenience.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) while they run: plug-ins
+ * whose host framework owns every device buffer, and latency-critical loops that
+ * forbid allocator calls after start-up.  This entry point takes the same inputs and
+ * outputs as fa_fwd_splitkv but no workspace: the partial results live in a fixed
+ * 64 MiB array inside the library (fa_noalloc_scratch_bytes()), which every GPU that
+ * loads the library holds until the process exits.
+ *
+ *   splits  as fa_fwd_splitkv (0 = automatic); when the split count needs more than
+ *           the built-in scratch, the call returns FA_ERR_UNSUPPORTED with a message
+ *           naming the limit, and launches nothing.
+ *
+ * The first call on a device (that needs more than one split) looks up the device
+ * address of the scratch array, once per device; make that first call before any
+ * stream capture.  The call allocates nothing.  All calls share the one array and it
+ * keeps the last call's contents; nothing in it needs to start at zero (every value
+ * the merge reads is written earlier in the same call).  Calls whose work overlaps on
+ * the GPU (for example on two streams at once) race on the array: serialise them.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                           int splits, void* stream);
+
+/* Size in bytes of the built-in scratch used by fa_fwd_splitkv_noalloc. */
+int64_t fa_noalloc_scratch_bytes(void);
+
 /* Static description of a status code. Never NULL. */
 const char* fa_strerror(int status);
 

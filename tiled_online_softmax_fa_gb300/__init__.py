@@ -14,7 +14,8 @@ import threading
 from . import build as _build
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_splitkv", "fa_fwd_splitkv_raw",
-           "splitkv_workspace_bytes", "splitkv_auto_splits", "get_device_status", "strerror", "last_error", "version",
+           "splitkv_workspace_bytes", "splitkv_auto_splits", "fa_fwd_splitkv_noalloc_raw",
+           "noalloc_scratch_bytes", "get_device_status", "strerror", "last_error", "version",
            "load_library", "FAError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED",
            "FA_ERR_MISALIGNED", "FA_ERR_ARCH", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
            "FwdOptions", "SUPPORTED_HEAD_DIMS"]
@@ -77,6 +78,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_int64
         lib.fa_splitkv_auto_splits.argtypes = [i64, i64, i64, ctypes.c_int]
         lib.fa_splitkv_auto_splits.restype = ctypes.c_int
+        lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64,
+                                               ctypes.c_int, ctypes.c_float, ctypes.c_int, vp]
+        lib.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
+        lib.fa_noalloc_scratch_bytes.argtypes = []
+        lib.fa_noalloc_scratch_bytes.restype = ctypes.c_int64
         _lib = lib
         return lib
 
@@ -198,6 +204,21 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, causal: bool = True, scale: float 
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_splitkv")
     return o, lse
+
+
+def fa_fwd_splitkv_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal, scale,
+                               splits, stream: int = 0) -> int:
+    """Split-KV forward using the library's built-in scratch (no workspace, no
+    allocation); raw device addresses in, status code out."""
+    lib = load_library()
+    return int(lib.fa_fwd_splitkv_noalloc(q_ptr or None, k_ptr or None, v_ptr or None,
+                                          o_ptr or None, lse_ptr or None, int(B), int(H), int(N),
+                                          int(d), int(bool(causal)), float(scale), int(splits),
+                                          stream or None))
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load_library().fa_noalloc_scratch_bytes())
 
 
 def get_device_status(stream=None) -> int:

@@ -14,6 +14,12 @@
 #include "fa_fwd_kernel.cuh"
 #include "fa_merge_kernel.cuh"
 
+// Built-in scratch for fa_fwd_splitkv_noalloc: callers that may not allocate device
+// memory get the split-KV workspace from this fixed array instead.  It is part of the
+// library's device image, so every GPU that loads the library holds it until exit.
+constexpr size_t kStaticScratchBytes = size_t{64} << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
 namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
@@ -341,6 +347,68 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int64_t N, int64_t d, int causal, float scale, void* stream) {
   return fa_fwd_opts(q, k, v, o, lse, B, H, N, d, causal, scale, stream, nullptr);
 }
+
+}  // extern "C"
+
+namespace {
+
+// Device address of g_static_scratch on the current device.  In host code the array's
+// name is only a stand-in, so the address is asked for once per device (with that
+// device current) and kept.
+void* g_scratch_ptr[kMaxDevices];
+bool g_scratch_ready[kMaxDevices];
+
+int static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return set_error(FA_ERR_UNSUPPORTED, "device index too large");
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ready[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_error("cudaGetSymbolAddress(static scratch)", e);
+    g_scratch_ptr[dev] = ptr;
+    g_scratch_ready[dev] = true;
+  }
+  *out = g_scratch_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                           int splits, void* stream) {
+  t_last_error.clear();
+  if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
+  if (head_dim_index(d) < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128");
+  if (splits < 0 || splits > kMaxSplits) return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
+  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (B > INT32_MAX / H || N > (int64_t{1} << 30))
+    return set_error(FA_ERR_UNSUPPORTED, "sizes beyond the kernel's range");
+  DeviceState* dev = nullptr;
+  int st = device_state(&dev);
+  if (st != FA_OK) return st;
+  if (splits == 0) splits = choose_splits(B * H, N, dev->num_sms, causal);
+  const int64_t need = workspace_bytes(B * H, N, d, splits);
+  if (need > static_cast<int64_t>(kStaticScratchBytes)) {
+    char buf[200];
+    snprintf(buf, sizeof buf,
+             "needs %lld bytes of scratch but the built-in scratch holds %zu (64 MiB); use "
+             "fa_fwd_splitkv with a workspace, or fewer splits",
+             static_cast<long long>(need), kStaticScratchBytes);
+    return set_error(FA_ERR_UNSUPPORTED, buf);
+  }
+  void* scratch = nullptr;
+  if (splits > 1 && (st = static_scratch_address(&scratch)) != FA_OK) return st;
+  return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, nullptr, splits, scratch,
+                 splits > 1 ? kStaticScratchBytes : 0);
+}
+
+int64_t fa_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kStaticScratchBytes); }
 
 const char* fa_strerror(int status) {
   switch (status) {
