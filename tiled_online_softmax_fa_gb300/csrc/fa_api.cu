@@ -159,9 +159,11 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   if ((st = encode_map(&mk, k, BH, N, HD)) != FA_OK) return st;
   if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
   if (!smem_set) {
-    const cudaError_t e = cudaFuncSetAttribute(fa_sm103::fa_fwd_kernel<HD>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(fa_sm103::fa_fwd_kernel<HD, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_sm103::fa_fwd_kernel<HD, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
     smem_set = true;
   }
@@ -192,7 +194,10 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   int grid = dev.num_sms;
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
   if (grid > p.num_items) grid = p.num_items;
-  fa_sm103::fa_fwd_kernel<HD><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  if (splits > 1)
+    fa_sm103::fa_fwd_kernel<HD, true><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  else
+    fa_sm103::fa_fwd_kernel<HD, false><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
   if (splits > 1) {

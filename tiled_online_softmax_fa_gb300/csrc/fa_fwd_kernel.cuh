@@ -139,15 +139,20 @@ __device__ __forceinline__ int tiles_for(int row_start, const Params& p) {
 struct Item {
   int bh, row0, k0, k1;
   int e[2];
+  // e[t] without a run-time array index (which would put the struct in local memory)
+  __device__ __forceinline__ int end(int t) const { return t == 0 ? e[0] : e[1]; }
 };
 
+// SPLIT = false compiles the unsplit kernel: an item is a whole unit, k0 = 0.
+template <bool SPLIT = true>
 __device__ __forceinline__ void item_coords(int w, const Params& p, Item& it) {
-  const int u = w / p.splits, sp = w - u * p.splits;
+  const int u = SPLIT ? w / p.splits : w;
+  const int sp = SPLIT ? w - u * p.splits : 0;
   unit_coords(u, p, it.bh, it.row0);
   const int n0 = tiles_for(it.row0, p), n1 = tiles_for(it.row0 + kBlockM, p);
   const int n = n0 > n1 ? n0 : n1;
-  it.k0 = sp * n / p.splits;
-  it.k1 = (sp + 1) * n / p.splits;
+  it.k0 = SPLIT ? sp * n / p.splits : 0;
+  it.k1 = SPLIT ? (sp + 1) * n / p.splits : n;
   it.e[0] = n0 < it.k1 ? n0 : it.k1;
   it.e[1] = n1 < it.k1 ? n1 : it.k1;
 }
@@ -178,7 +183,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* ptr) {
 // ------------------------------------------------------------------------------------
 // TMA producer (one lane)
 // ------------------------------------------------------------------------------------
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                           uint8_t* sQ, uint8_t* sRing, Barriers& b, const Params& p) {
   using C = Cfg<HD>;
@@ -192,7 +197,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
     const int u = unit_of(k);
     if (u >= p.num_items) continue;
     Item it;
-    item_coords(u, p, it);
+    item_coords<SPLIT>(u, p, it);
     if (it.k1 <= it.k0) continue;  // an empty KV range (more splits than tiles)
     const int bh = it.bh, row0 = it.row0;
     // Q smem is free once the previous item's last S MMA has completed
@@ -258,7 +263,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   }
 }
 
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b, const Params& p) {
   using C = Cfg<HD>;
   uint32_t ring = 0, units = 0;
@@ -270,7 +275,7 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
     const int u = unit_of(k);
     if (u >= p.num_items) continue;
     Item it;
-    item_coords(u, p, it);
+    item_coords<SPLIT>(u, p, it);
     if (it.k1 <= it.k0) continue;
     const int k0 = it.k0, k1 = it.k1;
     if (!wait_bar(&b.q_full, units & 1, p, b)) goto fail;
@@ -397,7 +402,7 @@ struct Xchg {
   float sum[2][2][2][kBlockM];    // [tile][half][exact|rounded][row]: partial row sums
 };
 
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = warp >> 3, h = (warp >> 2) & 1, wq = warp & 3;
@@ -415,8 +420,9 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& 
     const int u = unit_of(k);
     if (u >= p.num_items) continue;
     Item it;
-    item_coords(u, p, it);
-    if (it.e[t] <= it.k0) continue;  // this Q tile has no key tile in the item
+    item_coords<SPLIT>(u, p, it);
+    const int e_t = it.end(t);
+    if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
     const int bh = it.bh, row0 = it.row0;
     const int row_start = row0 + t * kBlockM;
     const int row = row_start + lrow;
@@ -424,7 +430,7 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& 
     const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
     float m_ref = -INFINITY;  // reference maximum, log2 units (identical in both halves)
     float l_exact = 0.f, l_round = 0.f;  // this half's partial sums
-    for (int j = it.k0; j < it.e[t]; ++j) {
+    for (int j = it.k0; j < e_t; ++j) {
       if (!warp_wait(&b.s_full[t], s_cnt & 1, p, b)) goto fail;
       tc_fence_after_sync();
       uint32_t s[64];
@@ -489,7 +495,7 @@ __device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& 
     if (!warp_wait(&b.o_full[t], o_cnt & 1, p, b)) goto fail;
     ++o_cnt;
     tc_fence_after_sync();
-    if (p.splits > 1) {
+    if constexpr (SPLIT) {
       // partial result of this KV range: normalised O (fp32) and its logsumexp
       const float inv_l = 1.f / l_round;
       const bool store = row < p.N;
@@ -544,7 +550,7 @@ fail:
 }
 
 // ------------------------------------------------------------------------------------
-template <int HD>
+template <int HD, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -585,13 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = b.tmem_base;
 
   if (warp < kSoftmaxWarps) {
-    softmax_role<HD>(tmem, b, xchg, p);
+    softmax_role<HD, SPLIT>(tmem, b, xchg, p);
   } else {
     if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<HD>(sQ, sRing, tmem, b, p);
+      if (lane == 0) mma_role<HD, SPLIT>(sQ, sRing, tmem, b, p);
       __syncwarp();
     } else if (warp == kLoadWarp) {
-      if (lane == 0) load_role<HD>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
+      if (lane == 0) load_role<HD, SPLIT>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
       __syncwarp();
     }
   }

@@ -33,8 +33,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   float m = -INFINITY;
   for (int sp = 0; sp < p.splits; ++sp) {
     Item it;
-    item_coords(u * p.splits + sp, p, it);
-    if (it.e[t] <= it.k0) continue;  // no key of this range is admissible for the row
+    item_coords<true>(u * p.splits + sp, p, it);
+    if (it.end(t) <= it.k0) continue;  // no key of this range is admissible for the row
     m = fmaxf(m, p.ws_lse[static_cast<size_t>(u * p.splits + sp) * kUnitRows + rin]);
   }
   float acc[E];
@@ -43,8 +43,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   float denom = 0.f;
   for (int sp = 0; sp < p.splits; ++sp) {
     Item it;
-    item_coords(u * p.splits + sp, p, it);
-    if (it.e[t] <= it.k0) continue;
+    item_coords<true>(u * p.splits + sp, p, it);
+    if (it.end(t) <= it.k0) continue;
     const size_t slot = static_cast<size_t>(u * p.splits + sp) * kUnitRows + rin;
     const float wgt = expf(p.ws_lse[slot] - m);
     denom += wgt;
