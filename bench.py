@@ -43,7 +43,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 SOURCES = ["tiled_online_softmax_fa_gb300/csrc/fa_api.cu",
            "tiled_online_softmax_fa_gb300/csrc/fa_fwd_kernel.cuh",
            "tiled_online_softmax_fa_gb300/csrc/ptx_sm103.cuh",
-           "tiled_online_softmax_fa_gb300/csrc/fa_merge_kernel.cuh"]
+           "tiled_online_softmax_fa_gb300/csrc/fa_merge_kernel.cuh",
+           "tiled_online_softmax_fa_gb300/csrc/fa_fwd_1tile_kernel.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
 
 

@@ -32,7 +32,7 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, non-finite or negative scale, aliasing */
-    FA_ERR_UNSUPPORTED = 2,    /* head dim not in {16, 32, 64, 128}, or a size beyond the kernel's range */
+    FA_ERR_UNSUPPORTED = 2,    /* head dim not in {16, 32, 64, 128, 256}, a split of head dim 256, or a size beyond the kernel's range */
     FA_ERR_MISALIGNED = 3,     /* a tensor base address not 16-byte aligned (lse: 4-byte) */
     FA_ERR_ARCH = 4,           /* current device is not compute capability 10.3 (sm_103) */
     FA_ERR_CUDA = 5,           /* a CUDA runtime / driver call failed; see fa_last_error() */
@@ -48,7 +48,9 @@ typedef enum {
  *            Written: o = softmax(scale q k^T + mask) v, rounded to bf16 (nearest even).
  *   lse      device pointer, fp32, [B, H, N] contiguous, or NULL to skip it.
  *   B, H, N  batch, heads, sequence length (queries = keys = N).  B*H*N == 0 is a no-op.
- *   d        head dimension, one of 16, 32, 64, 128.
+ *   d        head dimension, one of 16, 32, 64, 128, 256.  (256 runs a kernel with one
+ *            128-row query tile per work unit: 2 x 128 score columns + 256 output
+ *            columns fill the 512 tensor-memory columns of an SM.)
  *   causal   nonzero: query i attends keys j <= i (top-left aligned square mask).
  *   scale    finite, >= 0 (usually 1/sqrt(d)); applied to q.k before the softmax.
  *   stream   cudaStream_t to launch on (NULL = the legacy default stream).
@@ -97,7 +99,8 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
  * logsumexp of a union of key ranges), and it is what the lse output enables.
  *
  *   splits     1..64, or 0 to let the library choose (fa_splitkv_auto_splits);
- *              1 runs fa_fwd and needs no workspace.
+ *              1 runs fa_fwd and needs no workspace.  Head dim 256 has no split
+ *              variant: splits > 1 returns FA_ERR_UNSUPPORTED and 0 means 1.
  *   workspace  device memory, 16-byte aligned, caller-owned, at least
  *              fa_splitkv_workspace_bytes(B, H, N, d, splits) bytes (use the count from
  *              fa_splitkv_auto_splits for splits = 0); must not overlap any tensor.
@@ -108,7 +111,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
                    int splits, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes fa_fwd_splitkv needs for these sizes and `splits` (>= 1); -1 on bad arguments. */
+/* Workspace bytes fa_fwd_splitkv needs for these sizes and `splits` (>= 1); -1 on bad
+   arguments or an unsupported split (head dim 256 with splits > 1). */
 int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits);
 
 /*

@@ -55,7 +55,8 @@ def _call(**kw):
     (dict(B=-1), fa.FA_ERR_INVALID_ARG),
     (dict(N=-5), fa.FA_ERR_INVALID_ARG),
     (dict(d=48), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=192), fa.FA_ERR_UNSUPPORTED),
     (dict(q_ptr=0), fa.FA_ERR_INVALID_ARG),
     (dict(o_ptr=0), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
@@ -100,6 +101,8 @@ def test_splitkv_workspace_bytes():
     assert fa.splitkv_workspace_bytes(1, 32, 1024, 48, 4) == -1
     assert fa.splitkv_workspace_bytes(1, 32, 1024, 128, 0) == -1
     assert fa.splitkv_workspace_bytes(0, 32, 1024, 128, 4) == 0
+    assert fa.splitkv_workspace_bytes(1, 32, 1024, 256, 1) == 0
+    assert fa.splitkv_workspace_bytes(1, 32, 1024, 256, 4) == -1
 
 
 def _split(**kw):
@@ -117,6 +120,7 @@ def _split(**kw):
     (dict(splits=-1), fa.FA_ERR_INVALID_ARG),
     (dict(ws_ptr=0x20000), fa.FA_ERR_INVALID_ARG),      # workspace overlaps k
     (dict(d=40), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),             # no split variant for head dim 256
 ])
 def test_splitkv_argument_errors(kw, want):
     assert _split(**kw) == want

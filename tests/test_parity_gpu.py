@@ -70,7 +70,7 @@ def test_n32k_large_logits():
 # ---------------------------------------------------------------------------------------
 # shapes: ragged tails, tiny sequences, every head dim, several heads and batches
 # ---------------------------------------------------------------------------------------
-@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("N", [1, 2, 3, 127, 128, 129, 255, 256, 257, 383, 700])
 @pytest.mark.parametrize("causal", [True, False])
 def test_ragged_and_small(d, N, causal):
@@ -79,7 +79,7 @@ def test_ragged_and_small(d, N, causal):
     _parity.check_case(w, causal, B=2, H=3, N=N, d=d, seed=N * 7 + d, rows=rows)
 
 
-@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("d", [16, 64, 128, 256])
 def test_large_logits_ragged(d):
     _parity.check_case(W["n32k"], True, B=1, H=4, N=1000, d=d, seed=77 + d)
 

@@ -27,7 +27,7 @@ FA_ERR_MISALIGNED = 3
 FA_ERR_ARCH = 4
 FA_ERR_CUDA = 5
 FA_ERR_DEVICE_TIMEOUT = 6
-SUPPORTED_HEAD_DIMS = (16, 32, 64, 128)
+SUPPORTED_HEAD_DIMS = (16, 32, 64, 128, 256)
 
 
 class FwdOptions(ctypes.Structure):
@@ -122,7 +122,7 @@ def fa_fwd(q, k, v, o=None, lse=None, causal: bool = True, scale: float | None =
            want_lse: bool = True, stream=None, options: FwdOptions | None = None):
     """O = softmax(scale * q k^T + mask) v and its row logsumexp, on the GPU.
 
-    q, k, v : CUDA bf16 tensors [B, H, N, d], contiguous, d in {16, 32, 64, 128}.
+    q, k, v : CUDA bf16 tensors [B, H, N, d], contiguous, d in {16, 32, 64, 128, 256}.
     o, lse  : optional outputs ([B, H, N, d] bf16, [B, H, N] fp32); allocated if None.
     scale   : defaults to 1/sqrt(d), rounded to fp32.
     Returns (o, lse) (lse is None when ``want_lse`` is False and none was given).
@@ -188,7 +188,8 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, causal: bool = True, scale: float 
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    use = splits if splits > 0 else splitkv_auto_splits(B, H, N, causal)
+    # head dim 256 has no split variant: the automatic choice there is one piece
+    use = splits if splits > 0 else (1 if d == 256 else splitkv_auto_splits(B, H, N, causal))
     need = splitkv_workspace_bytes(B, H, N, d, use) if use > 1 else 0
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -11,6 +11,7 @@
 #include <string>
 
 #include "../../include/fa.h"
+#include "fa_fwd_1tile_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_merge_kernel.cuh"
 
@@ -47,7 +48,7 @@ struct DeviceState {
   bool probed = false;
   bool arch_ok = false;
   int num_sms = 0;
-  bool smem_set[4] = {false, false, false, false};
+  bool smem_set[5] = {false, false, false, false, false};
 };
 
 std::mutex g_mu;
@@ -60,6 +61,7 @@ int head_dim_index(int64_t d) {
     case 32: return 1;
     case 64: return 2;
     case 128: return 3;
+    case 256: return 4;
     default: return -1;
   }
 }
@@ -148,6 +150,41 @@ bool workspace_fits(const void* ws, size_t size, int64_t BH, int64_t N, int64_t 
   return true;
 }
 
+// Fields every launch shares.  `unit_rows` = query rows per work unit (256 for the
+// two-tile kernel, 128 for the head-dim-256 kernel).
+fa_sm103::Params base_params(void* o, float* lse, int64_t BH, int64_t N, int64_t d, int unit_rows,
+                             int causal, float scale, const fa_fwd_options* opts) {
+  fa_sm103::Params p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = static_cast<int>(BH);
+  p.N = static_cast<int>(N);
+  p.nkv = static_cast<int>((N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN);
+  p.nqb = static_cast<int>((N + unit_rows - 1) / unit_rows);
+  p.num_units = static_cast<int>(static_cast<int64_t>(p.nqb) * BH);
+  p.splits = 1;
+  p.num_items = p.num_units;
+  p.ws_o = nullptr;
+  p.ws_lse = nullptr;
+  // heads per scheduling group: their K and V together take at most ~64 MB of L2
+  const int64_t kv_bytes_per_head = 2 * N * d * 2;
+  int64_t g = (int64_t{64} << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  p.group_heads = static_cast<int>(g);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.budget = (opts && opts->wait_budget_cycles > 0) ? opts->wait_budget_cycles : kDefaultBudget;
+  p.inject = opts ? opts->inject_skip_kv_load : 0;
+  return p;
+}
+
+int grid_for(const DeviceState& dev, const fa_fwd_options* opts, int items) {
+  int grid = dev.num_sms;
+  if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
+  return grid > items ? items : grid;
+}
+
 template <int HD>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
            int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
@@ -167,33 +204,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
     smem_set = true;
   }
-  fa_sm103::Params p;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.BH = static_cast<int>(BH);
-  p.N = static_cast<int>(N);
-  p.nkv = static_cast<int>((N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN);
-  p.nqb = static_cast<int>((N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows);
-  p.num_units = static_cast<int>(static_cast<int64_t>(p.nqb) * BH);
+  fa_sm103::Params p = base_params(o, lse, BH, N, HD, fa_sm103::kUnitRows, causal, scale, opts);
   p.splits = splits;
   p.num_items = p.num_units * splits;
   p.ws_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
   p.ws_lse = splits > 1 ? static_cast<float*>(workspace) +
                               static_cast<size_t>(p.num_items) * fa_sm103::kUnitRows * HD
                         : nullptr;
-  // heads per scheduling group: their K and V together take at most ~64 MB of L2
-  const int64_t kv_bytes_per_head = 2 * N * HD * 2;
-  int64_t g = (int64_t{64} << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
-  if (g < 1) g = 1;
-  if (g > BH) g = BH;
-  p.group_heads = static_cast<int>(g);
-  p.causal = causal ? 1 : 0;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.budget = (opts && opts->wait_budget_cycles > 0) ? opts->wait_budget_cycles : kDefaultBudget;
-  p.inject = opts ? opts->inject_skip_kv_load : 0;
-  int grid = dev.num_sms;
-  if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
-  if (grid > p.num_items) grid = p.num_items;
+  const int grid = grid_for(dev, opts, p.num_items);
   if (splits > 1)
     fa_sm103::fa_fwd_kernel<HD, true><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   else
@@ -208,6 +226,32 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
   }
+  return FA_OK;
+}
+
+// Head dim 256: the one-Q-tile kernel (128-row units, no split-KV variant).
+int launch_d256(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
+                int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
+                bool& smem_set, const fa_fwd_options* opts) {
+  constexpr int HD = 256;
+  constexpr int SMEM = fa_sm103::one::Cfg1<HD>::SMEM_BYTES;
+  CUtensorMap mq, mk, mv;
+  int st;
+  if ((st = encode_map(&mq, q, BH, N, HD)) != FA_OK) return st;
+  if ((st = encode_map(&mk, k, BH, N, HD)) != FA_OK) return st;
+  if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
+  if (!smem_set) {
+    const cudaError_t e = cudaFuncSetAttribute(fa_sm103::one::fa_fwd_1tile_kernel<HD>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
+    smem_set = true;
+  }
+  const fa_sm103::Params p =
+      base_params(o, lse, BH, N, HD, fa_sm103::one::kUnitRows1, causal, scale, opts);
+  const int grid = grid_for(dev, opts, p.num_units);
+  fa_sm103::one::fa_fwd_1tile_kernel<HD><<<grid, fa_sm103::one::kThreads1, SMEM, stream>>>(mq, mk, mv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error("kernel launch", e);
   return FA_OK;
 }
 
@@ -244,10 +288,6 @@ int device_state(DeviceState** out) {
 
 }  // namespace
 
-extern "C" {
-
-}  // extern "C"
-
 namespace {
 
 // Shared body of every forward entry point.  splits = 0 chooses a split count (only
@@ -259,7 +299,7 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   // ---- pure argument checks: no CUDA call before these pass ----
   if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
   const int hd = head_dim_index(d);
-  if (hd < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128");
+  if (hd < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64, 128 or 256");
   if (B == 0 || H == 0 || N == 0) return FA_OK;  // nothing to compute
   if (!q || !k || !v || !o) return set_error(FA_ERR_INVALID_ARG, "null tensor pointer");
   if (!std::isfinite(scale) || scale < 0.f)
@@ -267,7 +307,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (B > INT32_MAX / H) return set_error(FA_ERR_UNSUPPORTED, "B*H too large");
   const int64_t BH = B * H;
   if (N > (int64_t{1} << 30)) return set_error(FA_ERR_UNSUPPORTED, "N too large");
-  const int64_t units = ((N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows) * BH;
+  const int64_t unit_rows = d == 256 ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
+  const int64_t units = ((N + unit_rows - 1) / unit_rows) * BH;
   if (units > INT32_MAX) return set_error(FA_ERR_UNSUPPORTED, "too many work units");
   if (BH > (INT64_MAX / 4) / (N * d)) return set_error(FA_ERR_UNSUPPORTED, "tensor too large");
   const size_t bytes = static_cast<size_t>(BH * N * d) * 2;
@@ -287,6 +328,10 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
     return set_error(FA_ERR_INVALID_ARG, "negative option");
   if (splits < 0 || splits > kMaxSplits)
     return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
+  if (d == 256) {
+    if (splits > 1) return set_error(FA_ERR_UNSUPPORTED, "split-KV is not available for head dim 256");
+    splits = 1;  // the automatic choice for head dim 256 is always one piece
+  }
   if (splits > 1 || (splits == 0 && workspace)) {
     if (!workspace) return set_error(FA_ERR_INVALID_ARG, "a split launch needs a workspace");
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
@@ -313,7 +358,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
     case 0: return launch<16>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
     case 1: return launch<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
     case 2: return launch<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
-    default: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    case 3: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    default: return launch_d256(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
   }
 }
 
@@ -330,6 +376,7 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
 int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits) {
   if (B < 0 || H < 0 || N < 0 || head_dim_index(d) < 0 || splits < 1 || splits > kMaxSplits)
     return -1;
+  if (d == 256 && splits > 1) return -1;  // no split-KV variant for head dim 256
   if (B == 0 || H == 0 || N == 0) return 0;
   return workspace_bytes(B * H, N, d, splits);
 }
@@ -389,15 +436,17 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
                            int splits, void* stream) {
   t_last_error.clear();
   if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
-  if (head_dim_index(d) < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64 or 128");
+  if (head_dim_index(d) < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64, 128 or 256");
   if (splits < 0 || splits > kMaxSplits) return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
+  if (d == 256 && splits > 1)
+    return set_error(FA_ERR_UNSUPPORTED, "split-KV is not available for head dim 256");
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   if (B > INT32_MAX / H || N > (int64_t{1} << 30))
     return set_error(FA_ERR_UNSUPPORTED, "sizes beyond the kernel's range");
   DeviceState* dev = nullptr;
   int st = device_state(&dev);
   if (st != FA_OK) return st;
-  if (splits == 0) splits = choose_splits(B * H, N, dev->num_sms, causal);
+  if (splits == 0) splits = d == 256 ? 1 : choose_splits(B * H, N, dev->num_sms, causal);
   const int64_t need = workspace_bytes(B * H, N, d, splits);
   if (need > static_cast<int64_t>(kStaticScratchBytes)) {
     char buf[200];

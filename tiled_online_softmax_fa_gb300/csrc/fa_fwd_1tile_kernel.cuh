@@ -1,0 +1,414 @@
+// fa_fwd_1tile_kernel.cuh -- the attention forward kernel for head dim 256.
+//
+// Same method and numerics as fa_fwd_kernel (blocked online softmax of the aiml.sh
+// "Speed up long contexts with FlashAttention" lab.py `tiled_flash_attention`, lazy
+// rescale, exact and bf16-rounded row sums), laid out for a 256-wide head:
+//   * Tensor memory (512 columns): S buffer 0 | S buffer 1 | O (256 fp32 columns).
+//     Two 128-row Q tiles (the other kernel's unit) would need 768 columns, so a work
+//     unit here is one (batch*head, 128-query-row tile).
+//   * The two S buffers let S(j+1) be computed while the softmax works on S(j): MMA
+//     order S(0), S(1), then for each KV tile j: PV(j), S(j+2).  P(j) is written over
+//     S buffer j % 2; S(j+2) reuses it only after PV(j) (MMAs of one thread run in
+//     order).  An O rescale first waits for PV(j-1) through a per-PV barrier.
+//   * Shared memory: one 64 KB Q tile and a 2-slot ring of 64 KB K/V tiles
+//     (192 KB + 1 KB alignment), filled by TMA with the 128-byte swizzle.
+//   * Warps (384 threads): 0-7 softmax (each row shared by two threads, one per half
+//     of the key columns, exchanging maxima and sums through shared memory), 8 MMA
+//     issuer, 9 TMA producer.  Every wait is bounded and sleeps.
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa_sm103 {
+namespace one {
+
+constexpr int kUnitRows1 = kBlockM;       // one Q tile per work unit
+constexpr int kSoftmaxWarps1 = 8;
+constexpr int kThreads1 = 384;
+constexpr int kMmaWarp1 = 8;
+constexpr int kLoadWarp1 = 9;
+constexpr uint32_t kSoftmaxThreads1 = 256;
+constexpr uint32_t kColS0_1 = 0, kColS1_1 = 128, kColO_1 = 256;
+
+template <int HD>
+struct Cfg1 {
+  static_assert(HD == 256, "the one-tile layout serves head dim 256");
+  using C = Cfg<HD>;
+  static constexpr int QBUF = 1;
+  static constexpr int NSLOT = 2;
+  static constexpr int SMEM_BYTES = (QBUF + NSLOT) * C::TILE_BYTES + 1024;
+};
+
+struct Barriers1 {
+  uint64_t q_full[2], q_empty[2];  // per Q buffer
+  uint64_t s_full[2], p_full[2];   // per S buffer
+  uint64_t pv_done;                // one completion per PV MMA group
+  uint64_t o_full, o_empty, drain;
+  uint64_t slot_full[8], slot_empty[8];
+  uint64_t pair[4];                // [row quadrant]: the two halves of a row meet here
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Xchg1 {
+  float mx[2][2][kBlockM];     // [parity][half][row]: partial row maxima
+  float sum[2][2][kBlockM];    // [half][exact|rounded][row]: partial row sums
+};
+
+// Unit u -> (head, first query row), the grouped longest-first order of unit_coords
+// with 128-row units (p.nqb = ceil(N / 128)).
+__device__ __forceinline__ void unit_coords1(int u, const Params& p, int& bh, int& row0) {
+  const int per_group = p.group_heads * p.nqb;
+  const int g = u / per_group;
+  const int first = g * p.group_heads;
+  const int heads = (p.BH - first) < p.group_heads ? (p.BH - first) : p.group_heads;
+  const int r = u - g * per_group;
+  const int qb = p.nqb - 1 - r / heads;
+  bh = first + r % heads;
+  row0 = qb * kUnitRows1;
+}
+
+__device__ __forceinline__ void raise_abort1(Barriers1& b) {
+  *reinterpret_cast<volatile int*>(&b.abort) = 1;
+  atomicOr(&g_device_status, 1u);
+}
+__device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, const Params& p, Barriers1& b) {
+  return mbar_wait_bounded(bar, parity, p.budget, &b.abort);
+}
+__device__ __forceinline__ bool warp_wait1(uint64_t* bar, uint32_t parity, const Params& p,
+                                           Barriers1& b) {
+  const bool ok = wait1(bar, parity, p, b);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// ------------------------------------------------------------------------------------
+// TMA producer (one lane).  Ring order per unit of n tiles: K0, K1, then for
+// j = 0 .. n-1: V_j, K_{j+2} (the order the MMA issuer consumes).
+// ------------------------------------------------------------------------------------
+struct RingState1 {
+  uint32_t ring = 0;
+  uint32_t skipped = 0xFFFFFFFFu;
+};
+
+template <int HD>
+__device__ __forceinline__ bool emit_kv1(const CUtensorMap* tm, int tile, int bh, int u,
+                                         uint8_t* sRing, Barriers1& b, const Params& p,
+                                         RingState1& rs) {
+  using C = Cfg<HD>;
+  constexpr int NS = Cfg1<HD>::NSLOT;
+  const uint32_t slot = rs.ring % NS, round = rs.ring / NS;
+  if (round > 0 && !wait1(&b.slot_empty[slot], (round - 1) & 1, p, b)) return false;
+  const bool skip = p.inject > 0 && u == 0 && rs.ring + 1 == static_cast<uint32_t>(p.inject);
+  if (skip) {
+    rs.skipped = rs.ring;
+  } else {
+    mbar_arrive_expect_tx(&b.slot_full[slot], C::TILE_BYTES);
+    for (int c = 0; c < C::NCH; ++c)
+      tma_load_3d(sRing + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, tm, &b.slot_full[slot],
+                  c * C::W, tile * kBlockN, bh);
+  }
+  ++rs.ring;
+  return true;
+}
+
+template <int HD>
+__device__ void load_role1(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                           uint8_t* sQ, uint8_t* sRing, Barriers1& b, const Params& p) {
+  using C = Cfg<HD>;
+  constexpr int QB = Cfg1<HD>::QBUF, NS = Cfg1<HD>::NSLOT;
+  prefetch_tmap(tmQ);
+  prefetch_tmap(tmK);
+  prefetch_tmap(tmV);
+  RingState1 rs;
+  uint32_t units = 0;
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_units) continue;
+    int bh, row0;
+    unit_coords1(u, p, bh, row0);
+    const int n = tiles_for(row0, p);
+    const uint32_t qb = units % QB;
+    // this Q buffer is free once the S MMAs of the unit that used it last are done
+    if (units >= QB && !wait1(&b.q_empty[qb], ((units / QB) - 1) & 1, p, b)) goto fail;
+    mbar_arrive_expect_tx(&b.q_full[qb], C::TILE_BYTES);
+    for (int c = 0; c < C::NCH; ++c)
+      tma_load_3d(sQ + qb * C::TILE_BYTES + c * C::CHUNK_BYTES, tmQ, &b.q_full[qb], c * C::W,
+                  row0, bh);
+    ++units;
+    if (!emit_kv1<HD>(tmK, 0, bh, u, sRing, b, p, rs)) goto fail;
+    if (n > 1 && !emit_kv1<HD>(tmK, 1, bh, u, sRing, b, p, rs)) goto fail;
+    for (int j = 0; j < n; ++j) {
+      if (!emit_kv1<HD>(tmV, j, bh, u, sRing, b, p, rs)) goto fail;
+      if (j + 2 < n && !emit_kv1<HD>(tmK, j + 2, bh, u, sRing, b, p, rs)) goto fail;
+    }
+  }
+  goto drain;
+fail:
+  raise_abort1(b);
+drain:
+  for (uint32_t i = rs.ring > NS ? rs.ring - NS : 0; i < rs.ring; ++i)
+    if (i != rs.skipped) drain_bar(&b.slot_full[i % NS], (i / NS) & 1, p);
+  for (uint32_t i = units > QB ? units - QB : 0; i < units; ++i)
+    drain_bar(&b.q_full[i % QB], (i / QB) & 1, p);
+}
+
+// ------------------------------------------------------------------------------------
+// MMA issuer (one lane)
+// ------------------------------------------------------------------------------------
+template <int HD>
+__device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1& b,
+                          const Params& p) {
+  using C = Cfg<HD>;
+  constexpr int QB = Cfg1<HD>::QBUF, NS = Cfg1<HD>::NSLOT;
+  uint32_t ring = 0, units = 0, oe_cnt = 0;
+  uint32_t p_cnt0 = 0, p_cnt1 = 0;  // p_full completions seen, per S buffer
+  const uint32_t ring_addr = smem_u32(sRing);
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_units) continue;
+    int bh, row0;
+    unit_coords1(u, p, bh, row0);
+    const int n = tiles_for(row0, p);
+    const uint32_t qb = units % QB;
+    const uint32_t q_addr = smem_u32(sQ + qb * C::TILE_BYTES);
+    if (!wait1(&b.q_full[qb], (units / QB) & 1, p, b)) goto fail;
+    ++units;
+    // S(0) and S(1) into the two S buffers
+    for (int j = 0; j < 2 && j < n; ++j) {
+      const uint32_t ks = ring % NS;
+      if (!wait1(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
+      ++ring;
+      tc_fence_after_sync();
+      issue_s<HD>(tmem + (j == 0 ? kColS0_1 : kColS1_1), q_addr, ring_addr + ks * C::TILE_BYTES);
+      mma_commit(&b.s_full[j]);
+      mma_commit(&b.slot_empty[ks]);
+    }
+    if (n <= 2) mma_commit(&b.q_empty[qb]);  // every S MMA of the unit is issued
+    for (int j = 0; j < n; ++j) {
+      const int sb = j & 1;
+      const uint32_t colS = sb == 0 ? kColS0_1 : kColS1_1;
+      const uint32_t vs = ring % NS;
+      if (!wait1(&b.slot_full[vs], (ring / NS) & 1, p, b)) goto fail;
+      ++ring;
+      if (j == 0) {  // O must have been read out by the previous unit's epilogue
+        if (!wait1(&b.o_empty, (oe_cnt & 1) ^ 1, p, b)) goto fail;
+        ++oe_cnt;
+      }
+      uint32_t& p_cnt = sb == 0 ? p_cnt0 : p_cnt1;
+      if (!wait1(&b.p_full[sb], p_cnt & 1, p, b)) goto fail;
+      ++p_cnt;
+      tc_fence_after_sync();
+      issue_pv<HD>(tmem + kColO_1, tmem + colS, ring_addr + vs * C::TILE_BYTES, j > 0);
+      mma_commit(&b.pv_done);
+      if (j == n - 1) mma_commit(&b.o_full);
+      mma_commit(&b.slot_empty[vs]);
+      if (j + 2 < n) {
+        const uint32_t ks = ring % NS;
+        if (!wait1(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
+        ++ring;
+        tc_fence_after_sync();
+        issue_s<HD>(tmem + colS, q_addr, ring_addr + ks * C::TILE_BYTES);
+        mma_commit(&b.s_full[sb]);
+        mma_commit(&b.slot_empty[ks]);
+        if (j + 2 == n - 1) mma_commit(&b.q_empty[qb]);
+      }
+    }
+  }
+  goto drain;
+fail:
+  raise_abort1(b);
+drain:
+  mma_commit(&b.drain);
+  drain_bar(&b.drain, 0, p);
+}
+
+// ------------------------------------------------------------------------------------
+// softmax / epilogue (warps 0-7)
+// ------------------------------------------------------------------------------------
+template <int HD>
+__device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Params& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = (warp >> 2) & 1, wq = warp & 3;
+  const int lrow = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tO = tmem + lane_base + kColO_1;
+  uint64_t* pair = &b.pair[wq];
+  const float c = p.scale_log2;
+  const uint64_t c2 = f32x2(c, c);
+  uint32_t s_cnt0 = 0, s_cnt1 = 0;  // s_full completions seen, per S buffer
+  uint32_t o_cnt = 0, x_cnt = 0, pv_cnt = 0;
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_units) continue;
+    int bh, row0;
+    unit_coords1(u, p, bh, row0);
+    const int n = tiles_for(row0, p);
+    const int row = row0 + lrow;
+    const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
+    float m_ref = -INFINITY;
+    float l_exact = 0.f, l_round = 0.f;
+    for (int j = 0; j < n; ++j, ++pv_cnt) {
+      const int sb = j & 1;
+      const uint32_t colS = sb == 0 ? kColS0_1 : kColS1_1;
+      uint32_t& s_cnt = sb == 0 ? s_cnt0 : s_cnt1;
+      if (!warp_wait1(&b.s_full[sb], s_cnt & 1, p, b)) goto fail;
+      ++s_cnt;
+      tc_fence_after_sync();
+      uint32_t s[64];
+      tmem_ld_x64(tmem + lane_base + colS + 64 * h, s);
+      tmem_wait_ld(s);
+      const int kv0 = j * kBlockN + 64 * h;
+      const int lim = last_key - kv0;
+      const bool warp_mask = __any_sync(0xFFFFFFFFu, kv0 + 63 > last_key);
+      const float pm = warp_mask ? row_max64<true>(s, lim) : row_max64<false>(s, lim);
+      x.mx[x_cnt & 1][h][lrow] = pm;
+      mbar_arrive(pair);
+      if (!warp_wait1(pair, x_cnt & 1, p, b)) goto fail;
+      const float mx = fmaxf(pm, x.mx[x_cnt & 1][h ^ 1][lrow]);
+      ++x_cnt;
+      const float mt = mx * c;
+      const bool need = mt > m_ref + kRescaleLog2;
+      const bool warp_rescale = __any_sync(0xFFFFFFFFu, need);
+      float alpha = 1.f;
+      if (need) {
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
+        m_ref = mt;
+        l_exact *= alpha;
+        l_round *= alpha;
+      }
+      const uint64_t negm2 = f32x2(-m_ref, -m_ref);
+      const uint32_t tP = tmem + lane_base + colS + 32 * h;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t pk[16];
+        const float2 sums = warp_mask ? exp_pack32<true>(s, pk, part, c2, negm2, lim)
+                                      : exp_pack32<false>(s, pk, part, c2, negm2, lim);
+        l_exact += sums.x;
+        l_round += sums.y;
+        tmem_st_x16(tP + 16 * part, pk);
+      }
+      if (warp_rescale && j > 0) {
+        // O holds the sum up to tile j-1 once PV(j-1) has completed
+        if (!warp_wait1(&b.pv_done, (pv_cnt - 1) & 1, p, b)) goto fail;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c0 = 32 * h; c0 < HD; c0 += 64) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_x32(tO + c0, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(&b.p_full[sb]);
+    }
+    // epilogue: O = acc / l_round in bf16, lse = (m_ref + log2 l_exact) ln 2
+    x.sum[h][0][lrow] = l_exact;
+    x.sum[h][1][lrow] = l_round;
+    mbar_arrive(pair);
+    if (!warp_wait1(pair, x_cnt & 1, p, b)) goto fail;
+    ++x_cnt;
+    l_exact += x.sum[h ^ 1][0][lrow];
+    l_round += x.sum[h ^ 1][1][lrow];
+    if (!warp_wait1(&b.o_full, o_cnt & 1, p, b)) goto fail;
+    ++o_cnt;
+    tc_fence_after_sync();
+    {
+      const float inv_l = 1.f / l_round;
+      const bool store = row < p.N;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + row) * HD;
+#pragma unroll
+      for (int c0 = 32 * h; c0 < HD; c0 += 64) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + c0, o);
+        tmem_wait_ld(o);
+        if (store) {
+#pragma unroll
+          for (int v8 = 0; v8 < 32; v8 += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[v8 + 0]) * inv_l, __uint_as_float(o[v8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[v8 + 2]) * inv_l, __uint_as_float(o[v8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[v8 + 4]) * inv_l, __uint_as_float(o[v8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[v8 + 6]) * inv_l, __uint_as_float(o[v8 + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + c0 + v8) = w;
+          }
+        }
+      }
+      if (h == 0 && store && p.lse != nullptr)
+        p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + lg2_approx(l_exact)) * kLn2;
+    }
+    tc_fence_before_sync();
+    mbar_arrive(&b.o_empty);
+  }
+  return;
+fail:
+  raise_abort1(b);
+}
+
+// ------------------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(kThreads1, 1)
+    fa_fwd_1tile_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<HD>;
+  constexpr int QB = Cfg1<HD>::QBUF, NS = Cfg1<HD>::NSLOT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + QB * C::TILE_BYTES;
+  __shared__ Barriers1 b;
+  __shared__ Xchg1 xchg;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    b.abort = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b.q_full[i], 1);
+      mbar_init(&b.q_empty[i], 1);
+      mbar_init(&b.s_full[i], 1);
+      mbar_init(&b.p_full[i], kSoftmaxThreads1);
+    }
+    mbar_init(&b.pv_done, 1);
+    mbar_init(&b.o_full, 1);
+    mbar_init(&b.o_empty, kSoftmaxThreads1);
+    mbar_init(&b.drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&b.pair[q], 64);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&b.slot_full[s], 1);
+      mbar_init(&b.slot_empty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp1) {
+    tmem_alloc(&b.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = b.tmem_base;
+
+  if (warp < kSoftmaxWarps1) {
+    softmax_role1<HD>(tmem, b, xchg, p);
+  } else if (warp == kMmaWarp1) {
+    if (lane == 0) mma_role1<HD>(sQ, sRing, tmem, b, p);
+    __syncwarp();
+  } else if (warp == kLoadWarp1) {
+    if (lane == 0) load_role1<HD>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace one
+}  // namespace fa_sm103

@@ -63,7 +63,7 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 template <int HD>
 struct Cfg {
-  static_assert(HD == 16 || HD == 32 || HD == 64 || HD == 128, "head dim");
+  static_assert(HD == 16 || HD == 32 || HD == 64 || HD == 128 || HD == 256, "head dim");
   static constexpr int W = HD < 64 ? HD : 64;          // elements per swizzled smem row
   static constexpr int SWB = 2 * W;                     // bytes per swizzled smem row
   static constexpr int NCH = HD / W;                    // row chunks across the head dim
