@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 SOURCES = [os.path.join(CSRC, "fa_api.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "fa_fwd_kernel.cuh"), os.path.join(CSRC, "ptx_sm103.cuh"),
                      os.path.join(CSRC, "fa_merge_kernel.cuh"), os.path.join(CSRC, "fa_fwd_1tile_kernel.cuh"),
+                     os.path.join(CSRC, "fa_fwd_row_kernel.cuh"),
                      os.path.join(ROOT, "include", "fa.h"), os.path.abspath(__file__)]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -13,6 +13,7 @@
 #include "../../include/fa.h"
 #include "fa_fwd_1tile_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_row_kernel.cuh"
 #include "fa_merge_kernel.cuh"
 
 // Built-in scratch for fa_fwd_splitkv_noalloc: callers that may not allocate device
@@ -196,10 +197,10 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   if ((st = encode_map(&mk, k, BH, N, HD)) != FA_OK) return st;
   if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
   if (!smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_sm103::fa_fwd_kernel<HD, false>,
+    cudaError_t e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fa_sm103::fa_fwd_kernel<HD, true>,
+      e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
     smem_set = true;
@@ -212,10 +213,11 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
                               static_cast<size_t>(p.num_items) * fa_sm103::kUnitRows * HD
                         : nullptr;
   const int grid = grid_for(dev, opts, p.num_items);
+  constexpr int kThr = fa_sm103::rowk::kThreadsR;
   if (splits > 1)
-    fa_sm103::fa_fwd_kernel<HD, true><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    fa_sm103::rowk::fa_fwd_row_kernel<HD, true><<<grid, kThr, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   else
-    fa_sm103::fa_fwd_kernel<HD, false><<<grid, fa_sm103::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    fa_sm103::rowk::fa_fwd_row_kernel<HD, false><<<grid, kThr, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
   if (splits > 1) {

@@ -14,7 +14,9 @@
 //     (192 KB + 1 KB alignment), filled by TMA with the 128-byte swizzle.
 //   * Warps (384 threads): 0-7 softmax (each row shared by two threads, one per half
 //     of the key columns, exchanging maxima and sums through shared memory), 8 MMA
-//     issuer, 9 TMA producer.  Every wait is bounded and sleeps.
+//     issuer, 9 TMA producer.  Every wait is bounded and sleeps.  Warps signal the
+//     barriers with one arrival each (lane 0 after __syncwarp); the sum of the rounded
+//     P is taken after P has been handed to the MMA.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -27,7 +29,6 @@ constexpr int kSoftmaxWarps1 = 8;
 constexpr int kThreads1 = 384;
 constexpr int kMmaWarp1 = 8;
 constexpr int kLoadWarp1 = 9;
-constexpr uint32_t kSoftmaxThreads1 = 256;
 constexpr uint32_t kColS0_1 = 0, kColS1_1 = 128, kColO_1 = 256;
 
 template <int HD>
@@ -66,6 +67,65 @@ __device__ __forceinline__ void unit_coords1(int u, const Params& p, int& bh, in
   const int qb = p.nqb - 1 - r / heads;
   bh = first + r % heads;
   row0 = qb * kUnitRows1;
+}
+
+// ------------------------------------------------------------------------------------
+// half-row softmax helpers: each query row is shared by two threads, one per 64-column
+// half of a 128-key score tile
+// ------------------------------------------------------------------------------------
+// P = 2^(s*c - m) on columns [32*part, 32*part + 32) of this thread's 64 (packed f32x2
+// FMA), rounded to bf16x2 into pk[16*part .. 16*part + 15].  `lim` = last admissible
+// column of the 64 (MASK).  Returns the sum of the fp32 P; the sum of the rounded P is
+// taken after P has been handed to the MMA (rounded_sum32).
+template <bool MASK>
+__device__ __forceinline__ float exp_pack32(const uint32_t (&s)[64], uint32_t (&pk)[32], int part,
+                                           uint64_t c2, uint64_t negm2, int lim) {
+  uint64_t esum[2] = {0, 0};  // two fp32 zeros each
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int col = 32 * part + 2 * i;
+    const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[col]), __uint_as_float(s[col + 1])), c2,
+                                 negm2);
+    float a0, a1;
+    f32x2_split(x, a0, a1);
+    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+    if (MASK) {
+      if (col > lim) p0 = 0.f;
+      if (col + 1 > lim) p1 = 0.f;
+    }
+    pk[16 * part + i] = pack_bf16x2(p0, p1);
+    esum[i & 1] = add_f32x2(esum[i & 1], f32x2(p0, p1));
+  }
+  float e0, e1, e2, e3;
+  f32x2_split(esum[0], e0, e1);
+  f32x2_split(esum[1], e2, e3);
+  return (e0 + e1) + (e2 + e3);
+}
+
+// Sum of the 64 bf16 values packed in pk (exact widening, fp32 additions).
+__device__ __forceinline__ float rounded_sum32(const uint32_t (&pk)[32]) {
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a[i & 3] = add_bf16x2_to_f32(a[i & 3], pk[i]);
+  return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
+template <bool MASK>
+__device__ __forceinline__ float row_max64(const uint32_t (&s)[64], int lim) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 64; i += 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float x0 = __uint_as_float(s[i + 2 * k]), x1 = __uint_as_float(s[i + 2 * k + 1]);
+      if (MASK) {
+        if (i + 2 * k > lim) x0 = -INFINITY;
+        if (i + 2 * k + 1 > lim) x1 = -INFINITY;
+      }
+      m[k] = max3(m[k], x0, x1);
+    }
+  }
+  return max3(m[0], m[1], fmaxf(m[2], m[3]));
 }
 
 __device__ __forceinline__ void raise_abort1(Barriers1& b) {
@@ -262,7 +322,8 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
       const bool warp_mask = __any_sync(0xFFFFFFFFu, kv0 + 63 > last_key);
       const float pm = warp_mask ? row_max64<true>(s, lim) : row_max64<false>(s, lim);
       x.mx[x_cnt & 1][h][lrow] = pm;
-      mbar_arrive(pair);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pair);
       if (!warp_wait1(pair, x_cnt & 1, p, b)) goto fail;
       const float mx = fmaxf(pm, x.mx[x_cnt & 1][h ^ 1][lrow]);
       ++x_cnt;
@@ -278,14 +339,12 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
       }
       const uint64_t negm2 = f32x2(-m_ref, -m_ref);
       const uint32_t tP = tmem + lane_base + colS + 32 * h;
+      uint32_t pk[32];  // P as bf16 pairs, kept for the rounded row sum below
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        uint32_t pk[16];
-        const float2 sums = warp_mask ? exp_pack32<true>(s, pk, part, c2, negm2, lim)
-                                      : exp_pack32<false>(s, pk, part, c2, negm2, lim);
-        l_exact += sums.x;
-        l_round += sums.y;
-        tmem_st_x16(tP + 16 * part, pk);
+        l_exact += warp_mask ? exp_pack32<true>(s, pk, part, c2, negm2, lim)
+                             : exp_pack32<false>(s, pk, part, c2, negm2, lim);
+        tmem_st_x16(tP + 16 * part, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * part]));
       }
       if (warp_rescale && j > 0) {
         // O holds the sum up to tile j-1 once PV(j-1) has completed
@@ -303,12 +362,16 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
       }
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(&b.p_full[sb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.p_full[sb]);
+      // off the critical path: the MMA already has P
+      l_round += rounded_sum32(pk);
     }
     // epilogue: O = acc / l_round in bf16, lse = (m_ref + log2 l_exact) ln 2
     x.sum[h][0][lrow] = l_exact;
     x.sum[h][1][lrow] = l_round;
-    mbar_arrive(pair);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pair);
     if (!warp_wait1(pair, x_cnt & 1, p, b)) goto fail;
     ++x_cnt;
     l_exact += x.sum[h ^ 1][0][lrow];
@@ -341,7 +404,8 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
         p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + lg2_approx(l_exact)) * kLn2;
     }
     tc_fence_before_sync();
-    mbar_arrive(&b.o_empty);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&b.o_empty);
   }
   return;
 fail:
@@ -370,13 +434,13 @@ __global__ void __launch_bounds__(kThreads1, 1)
       mbar_init(&b.q_full[i], 1);
       mbar_init(&b.q_empty[i], 1);
       mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_full[i], kSoftmaxThreads1);
+      mbar_init(&b.p_full[i], kSoftmaxWarps1);
     }
     mbar_init(&b.pv_done, 1);
     mbar_init(&b.o_full, 1);
-    mbar_init(&b.o_empty, kSoftmaxThreads1);
+    mbar_init(&b.o_empty, kSoftmaxWarps1);
     mbar_init(&b.drain, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&b.pair[q], 64);
+    for (int q = 0; q < 4; ++q) mbar_init(&b.pair[q], 2);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&b.slot_full[s], 1);
       mbar_init(&b.slot_empty[s], 1);

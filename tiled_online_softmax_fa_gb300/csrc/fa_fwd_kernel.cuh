@@ -1,4 +1,6 @@
-// fa_fwd_kernel.cuh -- the sm_103a attention forward kernel.
+// fa_fwd_kernel.cuh -- pieces shared by the sm_103a attention forward kernels: launch
+// parameters, work units and their order, the mbarrier set, the TMA producer and the
+// tcgen05 MMA issuer of the two-Q-tile kernel (fa_fwd_row_kernel.cuh).
 //
 // Method: the blocked online softmax of aiml.sh "Speed up long contexts with
 // FlashAttention" (lab.py, `tiled_flash_attention`): per query row a running maximum
@@ -13,12 +15,6 @@
 //     comfortably in L2, and inside a group the longest causal blocks first, so the
 //     units running at one time share a few heads' K/V through L2 and the per-CTA
 //     work evens out.
-//   * Warp roles (640 threads = 5 warpgroups): warps 0-7 = softmax for Q tile 0,
-//     warps 8-15 = softmax for Q tile 1 (two threads per query row, one per half of
-//     the key columns, in the same TMEM lane quadrant and SM sub-partition), warp 16 =
-//     tcgen05 MMA issuer (one lane), warp 17 = TMA producer (one lane), warps 18-19
-//     idle.  5 warps per SM sub-partition leave 96 registers a thread, enough for a
-//     half row of scores (64) and its packed P without spilling.
 //   * Shared memory: Q0, Q1 pinned for the unit; K and V tiles stream through an
 //     NSLOT-deep ring of 128-row slots filled by TMA (128/64/32-byte swizzle).
 //   * Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
@@ -51,11 +47,6 @@ __device__ unsigned int g_device_status;
 constexpr int kBlockM = 128;                // query rows per Q tile (TMEM lanes)
 constexpr int kBlockN = 128;                // keys per K/V tile
 constexpr int kUnitRows = 2 * kBlockM;      // query rows per work unit
-constexpr int kSoftmaxWarps = 16;
-constexpr int kThreads = 640;               // 16 softmax warps + 1 control warpgroup
-constexpr int kMmaWarp = 16;
-constexpr int kLoadWarp = 17;
-constexpr uint32_t kSoftmaxThreadsPerTile = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 constexpr float kRescaleLog2 = 8.0f;        // lazy-rescale threshold, log2 units
@@ -100,7 +91,7 @@ struct Barriers {
   uint64_t q_full, q_empty, drain;
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t slot_full[8], slot_empty[8];
-  uint64_t pair[2][4];          // [tile][row quadrant]: the two halves of a row meet here
+  uint64_t stats_full[2][2];    // [tile][unit parity]: row statistics handed to the epilogue
   uint32_t tmem_base;
   int abort;
 };
@@ -335,279 +326,11 @@ drain:
   drain_bar(&b.drain, 0, p);
 }
 
-// ------------------------------------------------------------------------------------
-// softmax / epilogue (warps 0-15).  Q tile t = warp / 8.  Each query row is shared by
-// two threads of the same TMEM lane quadrant (warp % 4) and SM sub-partition: the
-// thread in warp w takes key columns [64h, 64h + 64) with h = (warp / 4) % 2.  The two
-// halves exchange their row maxima (and, once per unit, their row sums) through
-// shared memory, synchronised by a 64-arrival mbarrier per row quadrant.
-// ------------------------------------------------------------------------------------
+// A bounded wait taken by a whole warp: true only if every lane saw the phase complete.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
                                           Barriers& b) {
   const bool ok = wait_bar(bar, parity, p, b);
   return __all_sync(0xFFFFFFFFu, ok);
-}
-
-// P = 2^(s*c - m) on columns [32*part, 32*part + 32) of this thread's 64 (packed f32x2
-// FMA), rounded to bf16x2 into pk.  `lim` = last admissible column of the 64 (MASK).
-// Returns {sum of the exact fp32 P, sum of the bf16-rounded P}.
-template <bool MASK>
-__device__ __forceinline__ float2 exp_pack32(const uint32_t (&s)[64], uint32_t (&pk)[16], int part,
-                                             uint64_t c2, uint64_t negm2, int lim) {
-  uint64_t esum = 0, rsum = 0;  // two fp32 zeros each
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int col = 32 * part + 2 * i;
-    const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[col]), __uint_as_float(s[col + 1])), c2,
-                                 negm2);
-    float a0, a1;
-    f32x2_split(x, a0, a1);
-    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-    if (MASK) {
-      if (col > lim) p0 = 0.f;
-      if (col + 1 > lim) p1 = 0.f;
-    }
-    const uint32_t w = pack_bf16x2(p0, p1);
-    pk[i] = w;
-    esum = add_f32x2(esum, f32x2(p0, p1));
-    rsum = add_f32x2(rsum, f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
-  }
-  float e0, e1, r0, r1;
-  f32x2_split(esum, e0, e1);
-  f32x2_split(rsum, r0, r1);
-  return make_float2(e0 + e1, r0 + r1);
-}
-
-template <bool MASK>
-__device__ __forceinline__ float row_max64(const uint32_t (&s)[64], int lim) {
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int i = 0; i < 64; i += 8) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float x0 = __uint_as_float(s[i + 2 * k]), x1 = __uint_as_float(s[i + 2 * k + 1]);
-      if (MASK) {
-        if (i + 2 * k > lim) x0 = -INFINITY;
-        if (i + 2 * k + 1 > lim) x1 = -INFINITY;
-      }
-      m[k] = max3(m[k], x0, x1);
-    }
-  }
-  return max3(m[0], m[1], fmaxf(m[2], m[3]));
-}
-
-// Exchange slots in shared memory (floats).
-struct Xchg {
-  float mx[2][2][2][kBlockM];     // [tile][parity][half][row]: partial row maxima
-  float sum[2][2][2][kBlockM];    // [tile][half][exact|rounded][row]: partial row sums
-};
-
-template <int HD, bool SPLIT>
-__device__ void softmax_role(uint32_t tmem, Barriers& b, Xchg& x, const Params& p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = warp >> 3, h = (warp >> 2) & 1, wq = warp & 3;
-  const int lrow = wq * 32 + lane;
-  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t colS = t == 0 ? kColS0 : kColS1;
-  const uint32_t tS = tmem + lane_base + colS + 64 * h;  // this thread's 64 score columns
-  const uint32_t tP = tmem + lane_base + colS + 32 * h;  // its 32 packed P columns
-  const uint32_t tO = tmem + lane_base + (t == 0 ? kColO0 : kColO1);
-  uint64_t* pair = &b.pair[t][wq];
-  const float c = p.scale_log2;
-  const uint64_t c2 = f32x2(c, c);
-  uint32_t s_cnt = 0, o_cnt = 0, x_cnt = 0;
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_items) continue;
-    Item it;
-    item_coords<SPLIT>(u, p, it);
-    const int e_t = it.end(t);
-    if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
-    const int bh = it.bh, row0 = it.row0;
-    const int row_start = row0 + t * kBlockM;
-    const int row = row_start + lrow;
-    // admissible keys for this row: j <= last_key
-    const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
-    float m_ref = -INFINITY;  // reference maximum, log2 units (identical in both halves)
-    float l_exact = 0.f, l_round = 0.f;  // this half's partial sums
-    for (int j = it.k0; j < e_t; ++j) {
-      if (!warp_wait(&b.s_full[t], s_cnt & 1, p, b)) goto fail;
-      tc_fence_after_sync();
-      uint32_t s[64];
-      tmem_ld_x64(tS, s);
-      tmem_wait_ld(s);
-      const int kv0 = j * kBlockN + 64 * h;
-      const int lim = last_key - kv0;               // last admissible column of the 64
-      const bool warp_mask = __any_sync(0xFFFFFFFFu, kv0 + 63 > last_key);
-      const float pm = warp_mask ? row_max64<true>(s, lim) : row_max64<false>(s, lim);
-      // combine with the other half of the row
-      x.mx[t][s_cnt & 1][h][lrow] = pm;
-      mbar_arrive(pair);
-      if (!warp_wait(pair, x_cnt & 1, p, b)) goto fail;
-      ++x_cnt;
-      const float mx = fmaxf(pm, x.mx[t][s_cnt & 1][h ^ 1][lrow]);
-      ++s_cnt;
-      const float mt = mx * c;
-      const bool need = mt > m_ref + kRescaleLog2;  // also true while m_ref is -inf
-      const bool warp_rescale = __any_sync(0xFFFFFFFFu, need);
-      float alpha = 1.f;
-      if (need) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
-        m_ref = mt;
-        l_exact *= alpha;
-        l_round *= alpha;
-      }
-      const uint64_t negm2 = f32x2(-m_ref, -m_ref);
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        uint32_t pk[16];
-        const float2 sums = warp_mask ? exp_pack32<true>(s, pk, part, c2, negm2, lim)
-                                      : exp_pack32<false>(s, pk, part, c2, negm2, lim);
-        l_exact += sums.x;
-        l_round += sums.y;
-        tmem_st_x16(tP + 16 * part, pk);
-      }
-      if (warp_rescale && j > it.k0) {
-        // PV_t(j-1) has completed (S_t(j) was issued after it) and PV_t(j) waits for
-        // this thread's arrival below: rescale this half's O chunks in place.
-#pragma unroll
-        for (int c0 = 32 * h; c0 < HD; c0 += 64) {
-          uint32_t o[32];
-          tmem_ld_x32(tO + c0, o);
-          tmem_wait_ld(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st_x32(tO + c0, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before_sync();
-      mbar_arrive(&b.p_full[t]);
-    }
-    // epilogue: O = acc / l_round in bf16, lse = (m_ref + log2 l_exact) ln 2
-    x.sum[t][h][0][lrow] = l_exact;
-    x.sum[t][h][1][lrow] = l_round;
-    mbar_arrive(pair);
-    if (!warp_wait(pair, x_cnt & 1, p, b)) goto fail;
-    ++x_cnt;
-    l_exact += x.sum[t][h ^ 1][0][lrow];
-    l_round += x.sum[t][h ^ 1][1][lrow];
-    if (!warp_wait(&b.o_full[t], o_cnt & 1, p, b)) goto fail;
-    ++o_cnt;
-    tc_fence_after_sync();
-    if constexpr (SPLIT) {
-      // partial result of this KV range: normalised O (fp32) and its logsumexp
-      const float inv_l = 1.f / l_round;
-      const bool store = row < p.N;
-      const size_t slot = static_cast<size_t>(u) * kUnitRows + t * kBlockM + lrow;
-      float* orow = p.ws_o + slot * HD;
-#pragma unroll
-      for (int c0 = 32 * h; c0 < HD; c0 += 64) {
-        uint32_t o[32];
-        tmem_ld_x32(tO + c0, o);
-        tmem_wait_ld(o);
-        if (store) {
-          constexpr int NV = HD < 32 ? HD : 32;
-#pragma unroll
-          for (int v4 = 0; v4 < NV; v4 += 4)
-            *reinterpret_cast<float4*>(orow + c0 + v4) =
-                make_float4(__uint_as_float(o[v4]) * inv_l, __uint_as_float(o[v4 + 1]) * inv_l,
-                            __uint_as_float(o[v4 + 2]) * inv_l, __uint_as_float(o[v4 + 3]) * inv_l);
-        }
-      }
-      if (h == 0 && store) p.ws_lse[slot] = (m_ref + lg2_approx(l_exact)) * kLn2;
-    } else {
-      const float inv_l = 1.f / l_round;
-      const bool store = row < p.N;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + row) * HD;
-#pragma unroll
-      for (int c0 = 32 * h; c0 < HD; c0 += 64) {
-        uint32_t o[32];
-        tmem_ld_x32(tO + c0, o);
-        tmem_wait_ld(o);
-        if (store) {
-          constexpr int NV = HD < 32 ? HD : 32;
-#pragma unroll
-          for (int v8 = 0; v8 < NV; v8 += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[v8 + 0]) * inv_l, __uint_as_float(o[v8 + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o[v8 + 2]) * inv_l, __uint_as_float(o[v8 + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o[v8 + 4]) * inv_l, __uint_as_float(o[v8 + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o[v8 + 6]) * inv_l, __uint_as_float(o[v8 + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + c0 + v8) = w;
-          }
-        }
-      }
-      if (h == 0 && store && p.lse != nullptr)
-        p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + lg2_approx(l_exact)) * kLn2;
-    }
-    tc_fence_before_sync();
-    mbar_arrive(&b.o_empty[t]);
-  }
-  return;
-fail:
-  raise_abort(b);
-}
-
-// ------------------------------------------------------------------------------------
-template <int HD, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using C = Cfg<HD>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint8_t* sQ = smem;
-  uint8_t* sRing = smem + C::SMEM_Q;
-  __shared__ Barriers b;
-  __shared__ Xchg xchg;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    b.abort = 0;
-    mbar_init(&b.q_full, 1);
-    mbar_init(&b.q_empty, 1);
-    mbar_init(&b.drain, 1);
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&b.s_full[t], 1);
-      mbar_init(&b.p_full[t], kSoftmaxThreadsPerTile);
-      mbar_init(&b.o_full[t], 1);
-      mbar_init(&b.o_empty[t], kSoftmaxThreadsPerTile);
-      for (int q = 0; q < 4; ++q) mbar_init(&b.pair[t][q], 64);
-    }
-    for (int s = 0; s < C::NSLOT; ++s) {
-      mbar_init(&b.slot_full[s], 1);
-      mbar_init(&b.slot_empty[s], 1);
-    }
-    fence_barrier_init();
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(&b.tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = b.tmem_base;
-
-  if (warp < kSoftmaxWarps) {
-    softmax_role<HD, SPLIT>(tmem, b, xchg, p);
-  } else {
-    if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<HD, SPLIT>(sQ, sRing, tmem, b, p);
-      __syncwarp();
-    } else if (warp == kLoadWarp) {
-      if (lane == 0) load_role<HD, SPLIT>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
-      __syncwarp();
-    }
-  }
-
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
-  }
 }
 
 }  // namespace fa_sm103

@@ -1,0 +1,361 @@
+// fa_fwd_row_kernel.cuh -- the attention forward kernel for head dims 16..128 with one
+// softmax thread per query row.
+//
+// Same method, work units, TMA producer and MMA issuer as fa_fwd_kernel (the blocked
+// online softmax of aiml.sh "Speed up long contexts with FlashAttention", lab.py
+// `tiled_flash_attention`: running maximum, running sum, accumulator rescaled when the
+// maximum grows, causal blocks above the diagonal skipped, the diagonal block masked).
+// What differs is how the softmax is laid out on the SM:
+//   * Warps (512 threads = 4 warpgroups): warpgroup 0 = softmax for Q tile 0,
+//     warpgroup 1 = softmax for Q tile 1, warpgroup 2 = epilogue (O / l, logsumexp,
+//     stores), warp 12 = tcgen05 MMA issuer (one lane), warp 13 = TMA producer (one
+//     lane), warps 14-15 idle.  Warp w reads TMEM lane quadrant w % 4, so every SM
+//     sub-partition holds one warp of each role.
+//   * Each softmax thread owns one query row and all 128 key columns of a score tile:
+//     the row maximum needs no exchange between threads.  Registers are moved to the
+//     softmax warpgroups with setmaxnreg (176 each; epilogue 72; control 88 -- the
+//     sum is exactly the 512 x 128 registers the block is launched with).
+//   * The epilogue warpgroup takes the finished accumulator O_t out of TMEM while the
+//     softmax warps already work on the next unit's first score tile.  Row statistics
+//     (reference maximum, exact and rounded row sums) pass through shared memory,
+//     double-buffered by unit parity.
+// Numerics are those of fa_fwd_kernel: exp2 with the scale folded into one FMA, lazy
+// rescale (threshold 8 in log2 units), P rounded to bf16 for the PV MMA, l_round (sum
+// of the rounded P) normalises O, l_exact gives the logsumexp.  l_round is summed from
+// the packed P after P has been handed to the MMA, so it stays off the chain
+// S ready -> P ready that the tensor core waits on.
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa_sm103 {
+namespace rowk {
+
+constexpr int kThreadsR = 512;
+constexpr int kEpilogueWarp0 = 8;
+constexpr int kMmaWarpR = 12;
+constexpr int kLoadWarpR = 13;
+// Barriers the softmax and epilogue warps signal take one arrival per warp (lane 0,
+// after __syncwarp): 128 per-thread arrivals on one shared-memory word are serialised
+// and were measured to cost ~500 cycles on the path S ready -> P ready.
+constexpr uint32_t kRowWarpsPerTile = 4;
+constexpr uint32_t kEpilogueWarps = 4;
+constexpr uint32_t kRegsSoftmax = 176, kRegsEpilogue = 72, kRegsControl = 88;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsEpilogue + 128 * kRegsControl <= kThreadsR * 128,
+              "register split exceeds the launch's registers");
+
+// Row statistics handed from a softmax thread to the epilogue thread of the same row.
+struct RowStats {
+  float m_ref[2][2][kBlockM];    // [tile][unit parity][row], log2 units
+  float l_exact[2][2][kBlockM];
+  float l_round[2][2][kBlockM];
+};
+
+// Row maximum of the 128 raw scores (columns > lim masked when MASK).
+template <bool MASK>
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[128], int lim) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 128; i += 16) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float x0 = __uint_as_float(s[i + 2 * k]), x1 = __uint_as_float(s[i + 2 * k + 1]);
+      if (MASK) {
+        if (i + 2 * k > lim) x0 = -INFINITY;
+        if (i + 2 * k + 1 > lim) x1 = -INFINITY;
+      }
+      m[k] = max3(m[k], x0, x1);
+    }
+  }
+  return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// P = 2^(s*c - m) for columns [32*part, 32*part + 32), packed to bf16x2 into
+// pk[16*part .. 16*part + 15].  Returns the sum of the fp32 P; two accumulators keep
+// the addition chain short.  The sum of the rounded P is taken later (rounded_sum64),
+// after P has been handed to the MMA.
+template <bool MASK>
+__device__ __forceinline__ float exp_pack32_row(const uint32_t (&s)[128], uint32_t (&pk)[64],
+                                                int part, uint64_t c2, uint64_t negm2, int lim) {
+  uint64_t esum[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int col = 32 * part + 2 * i;
+    const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[col]), __uint_as_float(s[col + 1])), c2,
+                                 negm2);
+    float a0, a1;
+    f32x2_split(x, a0, a1);
+    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+    if (MASK) {
+      if (col > lim) p0 = 0.f;
+      if (col + 1 > lim) p1 = 0.f;
+    }
+    pk[16 * part + i] = pack_bf16x2(p0, p1);
+    esum[i & 1] = add_f32x2(esum[i & 1], f32x2(p0, p1));
+  }
+  float e0, e1, e2, e3;
+  f32x2_split(esum[0], e0, e1);
+  f32x2_split(esum[1], e2, e3);
+  return (e0 + e1) + (e2 + e3);
+}
+
+// Sum of the 128 bf16 values packed in pk (exact widening, fp32 additions).
+__device__ __forceinline__ float rounded_sum64(const uint32_t (&pk)[64]) {
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 64; ++i) a[i & 3] = add_bf16x2_to_f32(a[i & 3], pk[i]);
+  return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
+// ------------------------------------------------------------------------------------
+// softmax (warpgroups 0 and 1): thread = one query row of Q tile t = warp / 4
+// ------------------------------------------------------------------------------------
+template <int HD, bool SPLIT>
+__device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const Params& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = warp >> 2, wq = warp & 3;
+  const int lrow = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_base + (t == 0 ? kColS0 : kColS1);
+  const uint32_t tO = tmem + lane_base + (t == 0 ? kColO0 : kColO1);
+  const float c = p.scale_log2;
+  const uint64_t c2 = f32x2(c, c);
+  uint32_t s_cnt = 0, u_cnt = 0;
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_items) continue;
+    Item it;
+    item_coords<SPLIT>(u, p, it);
+    const int e_t = it.end(t);
+    if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
+    const int row = it.row0 + t * kBlockM + lrow;
+    // admissible keys for this row: j <= last_key
+    const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
+    float m_ref = -INFINITY;  // reference maximum, log2 units
+    float l_exact = 0.f, l_round = 0.f;
+    for (int j = it.k0; j < e_t; ++j) {
+      if (!warp_wait(&b.s_full[t], s_cnt & 1, p, b)) goto fail;
+      ++s_cnt;
+      tc_fence_after_sync();
+      uint32_t s[128];
+      tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
+      tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&s[64]));
+      tmem_wait_ld(s);
+      const int kv0 = j * kBlockN;
+      const int lim = last_key - kv0;  // last admissible column of the tile
+      const bool warp_mask = __any_sync(0xFFFFFFFFu, kv0 + kBlockN - 1 > last_key);
+      const float mx = warp_mask ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
+      const float mt = mx * c;
+      const bool need = mt > m_ref + kRescaleLog2;  // also true while m_ref is -inf
+      const bool warp_rescale = __any_sync(0xFFFFFFFFu, need);
+      float alpha = 1.f;
+      if (need) {
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
+        m_ref = mt;
+        l_exact *= alpha;
+        l_round *= alpha;
+      }
+      const uint64_t negm2 = f32x2(-m_ref, -m_ref);
+      uint32_t pk[64];  // P as bf16 pairs, kept for the rounded row sum below
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        l_exact += warp_mask ? exp_pack32_row<true>(s, pk, part, c2, negm2, lim)
+                             : exp_pack32_row<false>(s, pk, part, c2, negm2, lim);
+        // P (bf16 pairs) over the first 64 columns of S
+        tmem_st_x16(tS + 16 * part, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * part]));
+      }
+      if (warp_rescale && j > it.k0) {
+        // PV_t(j-1) has completed (S_t(j) was issued after it) and PV_t(j) waits for
+        // this thread's arrival below: rescale this row of O in place.
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_x32(tO + c0, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.p_full[t]);
+      // off the critical path: the MMA already has P, the next S is not ready yet
+      l_round += rounded_sum64(pk);
+    }
+    {
+      // hand the row statistics to the epilogue (buffer = parity of this tile's units)
+      const int par = u_cnt & 1;
+      rs.m_ref[t][par][lrow] = m_ref;
+      rs.l_exact[t][par][lrow] = l_exact;
+      rs.l_round[t][par][lrow] = l_round;
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.stats_full[t][par]);
+      ++u_cnt;
+    }
+  }
+  return;
+fail:
+  raise_abort(b);
+}
+
+// ------------------------------------------------------------------------------------
+// epilogue (warpgroup 2): thread = one row of the Q tile being finished.  O = acc /
+// l_round rounded to bf16 (or, for a split item, the normalised fp32 partial O), and
+// lse = (m_ref + log2 l_exact) ln 2.
+// ------------------------------------------------------------------------------------
+template <int HD, bool SPLIT>
+__device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Params& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;
+  const int lrow = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  uint32_t cnt[2] = {0, 0};  // units finished per Q tile
+  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
+    const int u = unit_of(k);
+    if (u >= p.num_items) continue;
+    Item it;
+    item_coords<SPLIT>(u, p, it);
+#pragma unroll 1
+    for (int t = 0; t < 2; ++t) {
+      if (it.end(t) <= it.k0) continue;
+      const uint32_t c = t == 0 ? cnt[0] : cnt[1];
+      if (t == 0) ++cnt[0]; else ++cnt[1];
+      const int par = c & 1;
+      if (!warp_wait(&b.stats_full[t][par], (c >> 1) & 1, p, b)) goto fail;
+      const float m_ref = rs.m_ref[t][par][lrow];
+      const float l_exact = rs.l_exact[t][par][lrow];
+      const float l_round = rs.l_round[t][par][lrow];
+      if (!warp_wait(&b.o_full[t], c & 1, p, b)) goto fail;
+      tc_fence_after_sync();
+      const uint32_t tO = tmem + lane_base + (t == 0 ? kColO0 : kColO1);
+      const int row = it.row0 + t * kBlockM + lrow;
+      const bool store = row < p.N;
+      const float inv_l = 1.f / l_round;
+      constexpr int NV = HD < 32 ? HD : 32;  // columns of O per 32-column TMEM load
+      if constexpr (SPLIT) {
+        const size_t slot = static_cast<size_t>(u) * kUnitRows + t * kBlockM + lrow;
+        float* orow = p.ws_o + slot * HD;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          tmem_wait_ld(o);
+          if (store) {
+#pragma unroll
+            for (int v4 = 0; v4 < NV; v4 += 4)
+              *reinterpret_cast<float4*>(orow + c0 + v4) =
+                  make_float4(__uint_as_float(o[v4]) * inv_l, __uint_as_float(o[v4 + 1]) * inv_l,
+                              __uint_as_float(o[v4 + 2]) * inv_l, __uint_as_float(o[v4 + 3]) * inv_l);
+          }
+        }
+        if (store) p.ws_lse[slot] = (m_ref + lg2_approx(l_exact)) * kLn2;
+      } else {
+        __nv_bfloat16* orow = p.o + (static_cast<size_t>(it.bh) * p.N + row) * HD;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          tmem_wait_ld(o);
+          if (store) {
+#pragma unroll
+            for (int v8 = 0; v8 < NV; v8 += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[v8 + 0]) * inv_l, __uint_as_float(o[v8 + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[v8 + 2]) * inv_l, __uint_as_float(o[v8 + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[v8 + 4]) * inv_l, __uint_as_float(o[v8 + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[v8 + 6]) * inv_l, __uint_as_float(o[v8 + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + c0 + v8) = w;
+            }
+          }
+        }
+        if (store && p.lse != nullptr)
+          p.lse[static_cast<size_t>(it.bh) * p.N + row] = (m_ref + lg2_approx(l_exact)) * kLn2;
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.o_empty[t]);
+    }
+  }
+  return;
+fail:
+  raise_abort(b);
+}
+
+// ------------------------------------------------------------------------------------
+template <int HD, bool SPLIT>
+__global__ void __launch_bounds__(kThreadsR, 1)
+    fa_fwd_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const Params p) {
+  static_assert(HD <= 128, "the row kernel serves head dims 16..128");
+  using C = Cfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::SMEM_Q;
+  __shared__ Barriers b;
+  __shared__ RowStats rs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    b.abort = 0;
+    mbar_init(&b.q_full, 1);
+    mbar_init(&b.q_empty, 1);
+    mbar_init(&b.drain, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&b.s_full[t], 1);
+      mbar_init(&b.p_full[t], kRowWarpsPerTile);
+      mbar_init(&b.o_full[t], 1);
+      mbar_init(&b.o_empty[t], kEpilogueWarps);
+      mbar_init(&b.stats_full[t][0], kRowWarpsPerTile);
+      mbar_init(&b.stats_full[t][1], kRowWarpsPerTile);
+    }
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&b.slot_full[s], 1);
+      mbar_init(&b.slot_empty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarpR) {
+    tmem_alloc(&b.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = b.tmem_base;
+
+  if (warp < kEpilogueWarp0) {
+    setmaxnreg_inc<kRegsSoftmax>();
+    softmax_row_role<HD, SPLIT>(tmem, b, rs, p);
+    setmaxnreg_dec<128>();
+  } else if (warp < kMmaWarpR) {
+    setmaxnreg_dec<kRegsEpilogue>();
+    epilogue_role<HD, SPLIT>(tmem, b, rs, p);
+    setmaxnreg_inc<128>();
+  } else {
+    setmaxnreg_dec<kRegsControl>();
+    if (warp == kMmaWarpR) {
+      if (lane == 0) mma_role<HD, SPLIT>(sQ, sRing, tmem, b, p);
+      __syncwarp();
+    } else if (warp == kLoadWarpR) {
+      if (lane == 0) load_role<HD, SPLIT>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
+      __syncwarp();
+    }
+    setmaxnreg_inc<128>();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarpR) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace rowk
+}  // namespace fa_sm103

@@ -317,6 +317,18 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+// acc + lo + hi, where lo and hi are the two bf16 halves of w, each widened exactly and
+// added in fp32 (the mixed-precision add of sm_100-family SMs).
+__device__ __forceinline__ float add_bf16x2_to_f32(float acc, uint32_t w) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 %0, lo, %2;\n\t"
+      "add.rn.f32.bf16 %0, hi, %0;\n\t}"
+      : "=f"(r)
+      : "r"(w), "f"(acc));
+  return r;
+}
 // max of three fp32 values in one instruction
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
