@@ -44,7 +44,8 @@ SOURCES = ["tiled_online_softmax_fa_gb300/csrc/fa_api.cu",
            "tiled_online_softmax_fa_gb300/csrc/fa_fwd_kernel.cuh",
            "tiled_online_softmax_fa_gb300/csrc/ptx_sm103.cuh",
            "tiled_online_softmax_fa_gb300/csrc/fa_merge_kernel.cuh",
-           "tiled_online_softmax_fa_gb300/csrc/fa_fwd_1tile_kernel.cuh"]
+           "tiled_online_softmax_fa_gb300/csrc/fa_fwd_1tile_kernel.cuh",
+           "tiled_online_softmax_fa_gb300/csrc/fa_fwd_row_kernel.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
 
 
@@ -434,7 +435,8 @@ def run_ours(args):
                 "frac": kernel_tflops / peak, "traffic": traffic, "traffic_note": traffic_note,
                 "peak_source": peak_src, "algorithmic_flops_per_launch": flops,
                 "qkvo_compulsory_bytes_per_launch": 4 * B * H * N * d * 2 + B * H * N * 4,
-                "avg_launch_ms": ms_step, "kernel": f"fa_fwd_kernel<{d}>"}
+                "avg_launch_ms": ms_step,
+                "kernel": f"fa_fwd_row_kernel<{d}>" if d <= 128 else f"fa_fwd_1tile_kernel<{d}>"}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
