@@ -246,6 +246,8 @@ def parse_args(argv=None):
                     "1 = the unsplit kernel)")
     ap.add_argument("--sweep-launches", type=int, default=20, help="timed launches per length "
                     "(1 = a single untimed launch per length, for an ncu capture)")
+    ap.add_argument("--materialised", action="store_true", help="sweep: time the materialised "
+                    "baseline (S and P in device memory, cuBLAS GEMMs + row softmax) instead")
     return ap.parse_args(argv)
 
 
@@ -478,7 +480,12 @@ def run_sweep(args):
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         splits = args.splits if args.splits > 0 else fa.splitkv_auto_splits(B, H, N, causal)
-        if splits > 1:
+        if args.materialised:
+            splits = 1
+            ws = torch.empty(fa.materialised_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+            run = lambda: fa.fa_fwd_materialised(q, k, v, o=o, lse=lse, causal=causal,  # noqa: E731
+                                                 scale=scale, workspace=ws, stream=stream)
+        elif splits > 1:
             ws = torch.empty(fa.splitkv_workspace_bytes(B, H, N, d, splits), dtype=torch.uint8,
                              device=dev)
             run = lambda: fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, causal=causal, scale=scale,  # noqa: E731
@@ -486,6 +493,7 @@ def run_sweep(args):
         else:
             run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale, stream=stream)  # noqa: E731
         rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal, "splits": splits,
+               "path": "materialised" if args.materialised else "tiled",
                "flops": model_flops(B, H, N, d, causal)}
         if args.sweep_launches <= 1:
             run()
@@ -508,6 +516,7 @@ def run_sweep(args):
         results.append(rec)
         print(json.dumps(rec), flush=True)
         del q, k, v, o, lse
+        ws = None
         torch.cuda.empty_cache()
     peak, peak_src = load_peaks()
     with open(args.sweep, "w") as f:

@@ -15,8 +15,9 @@
  * rescaled when the maximum grows, so the score matrix never reaches device memory.
  * The logsumexp output is not on the pages; it is the plain definition above.
  *
- * All functions are plain C, take raw pointers and sizes, and never allocate
- * device memory.  Compute is asynchronous on the caller's stream.
+ * All functions are plain C and take raw pointers and sizes.  Compute is asynchronous
+ * on the caller's stream.  None allocates device memory, except that the first call of
+ * fa_fwd_materialised on a device creates a cuBLAS handle (see there).
  */
 #ifndef FA_SM103_H
 #define FA_SM103_H
@@ -150,6 +151,34 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 
 /* Size in bytes of the built-in scratch used by fa_fwd_splitkv_noalloc. */
 int64_t fa_noalloc_scratch_bytes(void);
+
+/*
+ * fa_fwd_materialised -- the materialised baseline: the same result computed the way the
+ * pages' `standard_attention` does it (aiml.sh "Speed up long contexts with
+ * FlashAttention", lab.py), with the N x N matrices in device memory:
+ *     S = scale * Q K^T            fp32 [B*H, N, N] in the workspace (cuBLAS batched GEMM)
+ *     P = exp(S - row max) + mask  bf16 [B*H, N, N] in the workspace, with the row sums
+ *                                  of the rounded P and lse = ln sum_j exp(s_j) (this
+ *                                  library's row kernel; masked entries are 0)
+ *     acc = P V                    fp32 [B*H, N, d] in the workspace (cuBLAS batched GEMM)
+ *     O = acc / row sum            bf16 (this library's kernel)
+ * It exists to measure the traffic and time the tiled kernels avoid (the pages model
+ * 4 H N^2 elements of such traffic per batch); it is not a fast path.
+ *
+ *   workspace  device memory, 256-byte aligned, caller-owned, at least
+ *              fa_materialised_workspace_bytes(B, H, N, d) (about 6 B H N^2 + 4 B H N d
+ *              bytes); must not overlap any tensor.  Its contents on entry do not matter.
+ * Other arguments and errors as fa_fwd (N up to 2^20 and B*H*N < 2^31 here).  Unlike the
+ * other entry points, the first call on a device creates a cuBLAS handle for it (cuBLAS
+ * allocates its own device workspace then); calls are serialised on a library lock.
+ */
+int fa_fwd_materialised(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_materialised needs (S, P, acc and row sums, each rounded up to a
+   multiple of 256 bytes); -1 on bad or too large sizes or an unsupported head dim. */
+int64_t fa_materialised_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
 
 /* Static description of a status code. Never NULL. */
 const char* fa_strerror(int status);

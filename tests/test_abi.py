@@ -125,3 +125,44 @@ def _split(**kw):
 def test_splitkv_argument_errors(kw, want):
     assert _split(**kw) == want
     assert fa.last_error() != ""
+
+
+def test_materialised_workspace_bytes():
+    def r256(x):
+        return (x + 255) // 256 * 256
+    # fp32 S | bf16 P ([B*H, N, N]) | fp32 acc [B*H, N, d] | fp32 row sums [B*H, N]
+    for B, H, N, d in ((1, 32, 1024, 128), (8, 32, 8192, 128), (2, 3, 129, 16)):
+        BH = B * H
+        want = r256(BH * N * N * 4) + r256(BH * N * N * 2) + r256(BH * N * d * 4) + r256(BH * N * 4)
+        assert fa.materialised_workspace_bytes(B, H, N, d) == want
+    assert fa.materialised_workspace_bytes(0, 32, 1024, 128) == 0
+    assert fa.materialised_workspace_bytes(-1, 32, 1024, 128) == -1
+    assert fa.materialised_workspace_bytes(1, 32, 1024, 40) == -1
+    assert fa.materialised_workspace_bytes(1, 1, (1 << 20) + 1, 128) == -1
+
+
+def _mat(**kw):
+    args = dict(q_ptr=0x10000, k_ptr=0x20000, v_ptr=0x30000, o_ptr=0x40000, lse_ptr=0, B=1, H=1,
+                N=128, d=64, causal=True, scale=0.1, ws_ptr=0x1000000, ws_bytes=10 ** 9)
+    args.update(kw)
+    return fa.fa_fwd_materialised_raw(**args)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ws_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=128 * 128 * 6), fa.FA_ERR_INVALID_ARG),    # no room for acc and row sums
+    (dict(ws_ptr=0x1000080), fa.FA_ERR_MISALIGNED),     # workspace must be 256-byte aligned
+    (dict(ws_ptr=0x20000 - 256), fa.FA_ERR_INVALID_ARG),  # workspace overlaps k
+    (dict(q_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(d=40), fa.FA_ERR_UNSUPPORTED),
+    (dict(o_ptr=0x40008), fa.FA_ERR_MISALIGNED),
+])
+def test_materialised_argument_errors(kw, want):
+    assert _mat(**kw) == want
+    assert fa.last_error() != ""
+
+
+def test_materialised_empty_is_a_noop():
+    assert _mat(B=0) == fa.FA_OK
+    assert _mat(N=0, ws_ptr=0) == fa.FA_OK

@@ -15,7 +15,8 @@ from . import build as _build
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_splitkv", "fa_fwd_splitkv_raw",
            "splitkv_workspace_bytes", "splitkv_auto_splits", "fa_fwd_splitkv_noalloc_raw",
-           "noalloc_scratch_bytes", "get_device_status", "strerror", "last_error", "version",
+           "noalloc_scratch_bytes", "fa_fwd_materialised", "fa_fwd_materialised_raw",
+           "materialised_workspace_bytes", "get_device_status", "strerror", "last_error", "version",
            "load_library", "FAError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED",
            "FA_ERR_MISALIGNED", "FA_ERR_ARCH", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
            "FwdOptions", "SUPPORTED_HEAD_DIMS"]
@@ -83,6 +84,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
         lib.fa_noalloc_scratch_bytes.argtypes = []
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_int64
+        lib.fa_fwd_materialised.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int,
+                                            ctypes.c_float, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_materialised.restype = ctypes.c_int
+        lib.fa_materialised_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        lib.fa_materialised_workspace_bytes.restype = ctypes.c_int64
         _lib = lib
         return lib
 
@@ -220,6 +226,53 @@ def fa_fwd_splitkv_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, 
 
 def noalloc_scratch_bytes() -> int:
     return int(load_library().fa_noalloc_scratch_bytes())
+
+
+def materialised_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_materialised_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_materialised_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal, scale,
+                            ws_ptr, ws_bytes, stream: int = 0) -> int:
+    """Call fa_fwd_materialised with raw device addresses; returns the status code."""
+    lib = load_library()
+    return int(lib.fa_fwd_materialised(q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None,
+                                       lse_ptr or None, int(B), int(H), int(N), int(d),
+                                       int(bool(causal)), float(scale), ws_ptr or None,
+                                       int(ws_bytes), stream or None))
+
+
+def fa_fwd_materialised(q, k, v, o=None, lse=None, causal: bool = True,
+                        scale: float | None = None, workspace=None, stream=None):
+    """The materialised baseline (N x N scores and probabilities in device memory).
+
+    ``workspace`` (a CUDA uint8 tensor of at least materialised_workspace_bytes) is
+    allocated here when not given.  Returns (o, lse).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 \
+                or t.dim() != 4 or not t.is_contiguous() or t.shape != q.shape:
+            raise TypeError(f"{name} must be a contiguous CUDA bf16 tensor shaped like q")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = materialised_workspace_bytes(B, H, N, d)
+    if need < 0:
+        raise FAError(FA_ERR_UNSUPPORTED, "fa_fwd_materialised")
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = fa_fwd_materialised_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, causal, scale, workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_materialised")
+    return o, lse
 
 
 def get_device_status(stream=None) -> int:

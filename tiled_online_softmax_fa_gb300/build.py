@@ -15,6 +15,7 @@ SOURCES = [os.path.join(CSRC, "fa_api.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "fa_fwd_kernel.cuh"), os.path.join(CSRC, "ptx_sm103.cuh"),
                      os.path.join(CSRC, "fa_merge_kernel.cuh"), os.path.join(CSRC, "fa_fwd_1tile_kernel.cuh"),
                      os.path.join(CSRC, "fa_fwd_row_kernel.cuh"),
+                     os.path.join(CSRC, "fa_materialised_kernel.cuh"),
                      os.path.join(ROOT, "include", "fa.h"), os.path.abspath(__file__)]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -43,7 +44,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB_PATH + f".{os.getpid()}.tmp"
     cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-           "-shared", "-o", tmp, *SOURCES]
+           "-shared", "-o", tmp, *SOURCES, "-lcublas"]
     if verbose:
         cmd[1:1] = ["-Xptxas", "-v"]
     res = subprocess.run(cmd, capture_output=True, text=True)
