@@ -40,11 +40,10 @@ import workloads  # noqa: E402
 METRIC = "FA fwd TFLOP/s (causal 2BHN²d) at b8 h32 S8192 d128 bf16; % of GB300 BF16 peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
-SOURCES = ["tiled_online_softmax_fa_gb300/csrc/fa_api.cu",
-           "tiled_online_softmax_fa_gb300/csrc/fa_fwd_kernel.cuh",
+# The device code of the kernel the bench line times (head dims 16-128): an ncu traffic
+# record applies only while these files are unchanged.
+SOURCES = ["tiled_online_softmax_fa_gb300/csrc/fa_fwd_kernel.cuh",
            "tiled_online_softmax_fa_gb300/csrc/ptx_sm103.cuh",
-           "tiled_online_softmax_fa_gb300/csrc/fa_merge_kernel.cuh",
-           "tiled_online_softmax_fa_gb300/csrc/fa_fwd_1tile_kernel.cuh",
            "tiled_online_softmax_fa_gb300/csrc/fa_fwd_row_kernel.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
 
