@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import _parity
+import oracle
 import tiled_online_softmax_fa_gb300 as fa
 import workloads
 
@@ -90,6 +91,40 @@ def test_many_units_per_cta():
     for causal in (True, False):
         rows = workloads.select_rows(W["b8n8k"], B=4, H=40, N=1536, seed=5)
         _parity.check_case(w, causal, B=4, H=40, N=1536, d=128, seed=5, rows=rows)
+
+
+def _sampled(N, per_head, BH, seed):
+    """Rows 0 and N-1 of every head plus `per_head` seeded random rows (unique, sorted)."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for bh in range(BH):
+        idx = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, per_head)]))
+        rows.extend((bh, int(i)) for i in idx)
+    return np.asarray(rows, dtype=np.int64)
+
+
+def test_longest_sequence_sampled_rows():
+    """N = 131072 (one head's K and V exceed the L2 share of a CTA group), unsplit and
+    split by key ranges; rows near the end attend to 131072 keys."""
+    w, N = W["n1k"], 131072
+    rows = _sampled(N, 24, 2, seed=131)
+    stats, (q, k, v, o, lse) = _parity.check_case(w, True, B=1, H=2, N=N, d=128, seed=131,
+                                                  rows=rows)
+    _report("N131072", stats)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    scale = float(np.float32(1.0 / np.sqrt(128)))
+    o2, l2 = fa.fa_fwd_splitkv(qd, kd, vd, causal=True, scale=scale, splits=0)
+    assert fa.get_device_status() == fa.FA_OK
+    og, lg = _parity.gather_rows(o2, l2, rows)
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, True, scale)
+    _parity.compare(og, lg, o64, lse64)
+
+
+def test_many_short_heads():
+    """B*H = 4096 one-tile units (far more units than CTAs, every unit a single block)."""
+    w = W["n1k"]
+    rows = _sampled(64, 2, 64 * 64, seed=9)[::7]
+    _parity.check_case(w, True, B=64, H=64, N=64, d=64, seed=9, rows=rows)
 
 
 # ---------------------------------------------------------------------------------------
