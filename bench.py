@@ -193,6 +193,20 @@ def oracle_rows_flops(rows: np.ndarray, N: int, d: int, causal: bool) -> float:
     return float(4.0 * d * keys.sum())
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo; 'unknown' where it says none)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "CPU part"):
+        for line in text.splitlines():
+            if line.startswith(key) and ":" in line:
+                return f"{line.split(':', 1)[1].strip()} ({os.cpu_count()} cpus)"
+    return f"unknown ({os.cpu_count()} cpus)"
+
+
 def time_oracle(q, k, v, causal, scale, seconds: float, seed: int = 12345):
     """Run the oracle on seeded random query rows for about `seconds` of wall time.
 
@@ -284,7 +298,10 @@ def run_reference(args):
                    "causal": causal, "step": "fp64 CPU oracle over a bounded random-row sample"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{rows_total} random query rows over {args.steps} steps "
-                                   f"(~{per_step:.2f} s each) of the {name} workload"},
+                                   f"(~{per_step:.2f} s each) of the {name} workload",
+                         "cpu_model": cpu_model(),
+                         "full_workload_s_extrapolated":
+                             model_flops(args.B, args.H, args.N, args.d, causal) / (value * 1e12)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -443,7 +460,9 @@ def run_ours(args):
     if not args.no_cpu_baseline and world == 1:
         val, rows, el, threads = time_oracle(q, k, v, causal, scale, args.cpu_seconds)
         cpu = {"value": val / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{rows} random query rows of the {name} workload, fp64, {el:.1f} s"}
+               "sample": f"{rows} random query rows of the {name} workload, fp64, {el:.1f} s",
+               "cpu_model": cpu_model(),
+               "full_workload_s_extrapolated": flops / val}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
