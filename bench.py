@@ -255,8 +255,12 @@ def parse_args(argv=None):
     ap.add_argument("--sweep", default="", help="write a sequence-length sweep (JSON) to this path "
                     "instead of the contract line")
     ap.add_argument("--sweep-n", default="512,1024,2048,4096,8192,16384,32768,65536,131072")
-    ap.add_argument("--splits", type=int, default=1, help="sweep: key-range splits (0 = auto, "
-                    "1 = the unsplit kernel)")
+    ap.add_argument("--splits", type=int, default=1, help="sweep: key-range splits (0 = the "
+                    "library's plan with splitting allowed, 1 = unsplit)")
+    ap.add_argument("--kernel", choices=["auto", "two", "one"], default="auto",
+                    help="sweep, unsplit: pin the two-tile or the one-tile kernel")
+    ap.add_argument("--sweep-shapes", default="", help="sweep: 'B,H,N;B,H,N;...' (overrides "
+                    "--B, --H and --sweep-n)")
     ap.add_argument("--sweep-launches", type=int, default=20, help="timed launches per length "
                     "(1 = a single untimed launch per length, for an ncu capture)")
     ap.add_argument("--materialised", action="store_true", help="sweep: time the materialised "
@@ -454,7 +458,8 @@ def run_ours(args):
                 "peak_source": peak_src, "algorithmic_flops_per_launch": flops,
                 "qkvo_compulsory_bytes_per_launch": 4 * B * H * N * d * 2 + B * H * N * 4,
                 "avg_launch_ms": ms_step,
-                "kernel": f"fa_fwd_row_kernel<{d}>" if d <= 128 else f"fa_fwd_1tile_kernel<{d}>"}
+                "kernel": ("fa_fwd_1tile_kernel" if fa.fwd_plan(B, H, N, d, causal)[0] ==
+                           fa.FA_KERNEL_ONE_TILE else "fa_fwd_row_kernel") + f"<{d}>"}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -493,11 +498,25 @@ def run_sweep(args):
     scale = float(np.float32(1.0 / np.sqrt(d)))
     stream = torch.cuda.current_stream(dev)
     results = []
-    for N in [int(x) for x in args.sweep_n.split(",")]:
+    if args.sweep_shapes:
+        shapes = [tuple(int(x) for x in t.split(",")) for t in args.sweep_shapes.split(";") if t]
+    else:
+        shapes = [(B, H, int(x)) for x in args.sweep_n.split(",")]
+    pin = {"auto": fa.FA_KERNEL_AUTO, "two": fa.FA_KERNEL_TWO_TILE, "one": fa.FA_KERNEL_ONE_TILE}
+    for B, H, N in shapes:
         q, k, v = (t.to(dev) for t in workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=7000 + N))
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        splits = args.splits if args.splits > 0 else fa.splitkv_auto_splits(B, H, N, causal)
+        kernel = pin[args.kernel]
+        if args.splits == 0:
+            kernel, splits = fa.fwd_plan(B, H, N, d, causal, allow_split=True)
+        else:
+            splits = args.splits
+            if splits == 1 and kernel == fa.FA_KERNEL_AUTO:
+                kernel = fa.fwd_plan(B, H, N, d, causal)[0]
+            elif splits > 1:
+                kernel = fa.FA_KERNEL_TWO_TILE
+        opts = fa.FwdOptions(kernel=kernel) if splits == 1 else None
         if args.materialised:
             splits = 1
             ws = torch.empty(fa.materialised_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
@@ -509,8 +528,11 @@ def run_sweep(args):
             run = lambda: fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, causal=causal, scale=scale,  # noqa: E731
                                             splits=splits, workspace=ws, stream=stream)
         else:
-            run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale, stream=stream)  # noqa: E731
+            run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale,  # noqa: E731
+                                    stream=stream, options=opts)
         rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal, "splits": splits,
+               "kernel": None if args.materialised else
+               {fa.FA_KERNEL_TWO_TILE: "two-tile", fa.FA_KERNEL_ONE_TILE: "one-tile"}[kernel],
                "path": "materialised" if args.materialised else "tiled",
                "flops": model_flops(B, H, N, d, causal)}
         if args.sweep_launches <= 1:

@@ -51,7 +51,8 @@ typedef enum {
  *   B, H, N  batch, heads, sequence length (queries = keys = N).  B*H*N == 0 is a no-op.
  *   d        head dimension, one of 16, 32, 64, 128, 256.  (256 runs a kernel with one
  *            128-row query tile per work unit: 2 x 128 score columns + 256 output
- *            columns fill the 512 tensor-memory columns of an SM.)
+ *            columns fill the 512 tensor-memory columns of an SM.  At 128 the library
+ *            picks that kernel or the two-tile one per call; see fa_fwd_plan.)
  *   causal   nonzero: query i attends keys j <= i (top-left aligned square mask).
  *   scale    finite, >= 0 (usually 1/sqrt(d)); applied to q.k before the softmax.
  *   stream   cudaStream_t to launch on (NULL = the legacy default stream).
@@ -77,12 +78,30 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *                       bounded wait must run out (host-side fault injection; no
  *                       GPU fault is involved).  0 = off.
  *   max_ctas            cap on the persistent grid (0 = one CTA per SM).
+ *   kernel              FA_KERNEL_AUTO (0): the library's choice (fa_fwd_plan);
+ *                       FA_KERNEL_TWO_TILE or FA_KERNEL_ONE_TILE pins that kernel
+ *                       (FA_ERR_UNSUPPORTED for a head dim it does not serve).
+ *   reserved            must be 0.
  */
 typedef struct {
     int64_t wait_budget_cycles;
     int32_t inject_skip_kv_load;
     int32_t max_ctas;
+    int32_t kernel;
+    int32_t reserved;
 } fa_fwd_options;
+
+/*
+ * The forward kernels.  Both compute the same result with the same arithmetic; they
+ * differ in the query rows of one work unit (one unit per CTA at a time, units handed
+ * out in a fixed longest-first order over a persistent grid of one CTA per SM).
+ */
+typedef enum {
+    FA_KERNEL_AUTO = 0,
+    FA_KERNEL_TWO_TILE = 1,  /* 256 query rows per unit (two 128-row Q tiles sharing each
+                                K/V tile); head dims 16-128; the only one with split-KV */
+    FA_KERNEL_ONE_TILE = 2   /* 128 query rows per unit; head dims 128 and 256 */
+} fa_kernel;
 
 /* fa_fwd with options; opts may be NULL (same as fa_fwd). */
 int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -99,12 +118,13 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
  * The pages do not describe this; it follows from the definition above (the
  * logsumexp of a union of key ranges), and it is what the lse output enables.
  *
- *   splits     1..64, or 0 to let the library choose (fa_splitkv_auto_splits);
+ *   splits     1..64, or 0 to let the library choose (fa_fwd_plan with allow_split);
  *              1 runs fa_fwd and needs no workspace.  Head dim 256 has no split
  *              variant: splits > 1 returns FA_ERR_UNSUPPORTED and 0 means 1.
  *   workspace  device memory, 16-byte aligned, caller-owned, at least
- *              fa_splitkv_workspace_bytes(B, H, N, d, splits) bytes (use the count from
- *              fa_splitkv_auto_splits for splits = 0); must not overlap any tensor.
+ *              fa_splitkv_workspace_bytes(B, H, N, d, splits) bytes (for splits = 0,
+ *              the count from fa_fwd_plan or fa_splitkv_auto_splits, which is never
+ *              smaller); must not overlap any tensor.
  *              Its contents on entry do not matter; they are scratch after the call.
  * Other arguments, ownership and errors as fa_fwd.
  */
@@ -117,11 +137,37 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits);
 
 /*
- * The split count fa_fwd_splitkv uses for splits = 0 on the current device (1 on error):
- * more than one only when the longest query block's key range would be the critical
- * path (few, long blocks for the number of SMs, e.g. one head at N = 32768).
+ * The split count the two-tile kernel takes for splits = 0 on the current device (1 on
+ * error): more than one only when the longest query block's key range would be the
+ * critical path (few, long blocks for the number of SMs, e.g. one head at N = 32768).
+ * At head dim 128 fa_fwd_plan may still run such a call unsplit on the one-tile
+ * kernel; a workspace sized for this count always suffices.
  */
 int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
+
+/*
+ * fa_fwd_plan -- the launch the library picks for these sizes: which kernel
+ * (FA_KERNEL_TWO_TILE or FA_KERNEL_ONE_TILE, written to *kernel) and how many key-range
+ * pieces (*splits; 1 = unsplit).  allow_split = 0 gives fa_fwd's choice, nonzero the
+ * choice of fa_fwd_splitkv / fa_fwd_splitkv_noalloc with splits = 0.  num_sms = 0 asks
+ * the current device for its SM count (a CUDA call); > 0 plans for that many SMs
+ * without touching CUDA.
+ *
+ * Head dims 16-64 always take the two-tile kernel and 256 the one-tile kernel.  At 128,
+ * when there are at most four 256-row units per SM, the library models the run time of
+ * each candidate -- the two-tile kernel unsplit, split as fa_splitkv_auto_splits says,
+ * and the one-tile kernel -- by replaying the kernels' static schedule (unit lengths in
+ * key tiles; a one-tile kernel tile costing 1.18 two-tile tiles; fixed costs of 1 tile
+ * per unsplit two-tile unit and 6 per split piece; the merge 5 tiles plus 1 per MB of
+ * partial results; all fitted to GB300 timings) and takes the shortest.  Few long units (one head at N = 8192) go
+ * to the one-tile kernel, whose half-size units spread the causal triangle more evenly.
+ *
+ * Returns FA_OK, FA_ERR_INVALID_ARG (negative size, null output pointer) or
+ * FA_ERR_UNSUPPORTED (head dim); an empty problem plans (FA_KERNEL_TWO_TILE, 1), or
+ * (FA_KERNEL_ONE_TILE, 1) at head dim 256.
+ */
+int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allow_split,
+                int num_sms, int* kernel, int* splits);
 
 /*
  * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that may not allocate device

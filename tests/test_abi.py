@@ -25,7 +25,7 @@ def _declared_functions():
 def test_library_builds_and_loads():
     lib = fa.load_library()
     assert isinstance(lib, ctypes.CDLL)
-    assert fa.version() == 100
+    assert fa.version() == 200
 
 
 def test_every_declared_symbol_is_exported():

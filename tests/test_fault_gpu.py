@@ -24,17 +24,19 @@ def _need_gpu():
     fa.load_library()
 
 
-@pytest.mark.parametrize("d", [128, 256])
-def test_skipped_load_times_out_and_context_survives(d):
-    """d = 128 runs the two-tile kernel, d = 256 the one-tile kernel (its own ring order)."""
+@pytest.mark.parametrize("d,kernel", [(128, fa.FA_KERNEL_TWO_TILE), (128, fa.FA_KERNEL_ONE_TILE),
+                                      (256, fa.FA_KERNEL_ONE_TILE)])
+def test_skipped_load_times_out_and_context_survives(d, kernel):
+    """Both kernels (the one-tile kernel has its own ring order and, at d = 128, two Q
+    buffers and four ring slots to drain)."""
     w = workloads.WORKLOADS["n1k"]
     q, k, v = workloads.make_inputs(w, B=1, H=2, N=1024, d=d, seed=21)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     assert fa.get_device_status() == fa.FA_OK  # clean start
-    opts = fa.FwdOptions(wait_budget_cycles=20_000_000, inject_skip_kv_load=3)
+    opts = fa.FwdOptions(wait_budget_cycles=20_000_000, inject_skip_kv_load=3, kernel=kernel)
     fa.fa_fwd(qd, kd, vd, causal=True, options=opts)
     assert fa.get_device_status() == fa.FA_ERR_DEVICE_TIMEOUT
     # the status word was cleared by the read, and the next call is correct
-    stats, _ = _parity.check_case(w, True, B=1, H=2, N=1024, d=d, seed=21)
+    stats, _ = _parity.check_case(w, True, B=1, H=2, N=1024, d=d, seed=21, kernel=kernel)
     assert fa.get_device_status() == fa.FA_OK
     assert stats["o_max_abs"] < 8e-3

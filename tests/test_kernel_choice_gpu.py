@@ -1,0 +1,123 @@
+"""GPU parity of both head-dim-128 kernels and of the launch the planner picks.
+
+At head dim 128 a call runs either the two-tile kernel (256-row units) or the
+one-tile kernel (128-row units), whichever fa_fwd_plan models as faster; small
+problems go to the one-tile kernel.  Each kernel is pinned here through
+fa_fwd_options.kernel and compared with the fp64 oracle on the same seeded inputs,
+so both stay covered whatever the planner picks for the other tests' shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _parity
+import oracle
+import tiled_online_softmax_fa_gb300 as fa
+import workloads
+
+pytestmark = pytest.mark.gpu
+W = workloads.WORKLOADS
+TWO, ONE = fa.FA_KERNEL_TWO_TILE, fa.FA_KERNEL_ONE_TILE
+KERNELS = [pytest.param(TWO, id="two-tile"), pytest.param(ONE, id="one-tile")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.load_library()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 256, 257, 383, 700, 1000])
+@pytest.mark.parametrize("causal", [True, False])
+def test_pinned_ragged_and_small(kernel, N, causal):
+    w = W["n1k"]
+    rows = workloads.select_rows(w, B=2, H=3, N=N, seed=N + 128)
+    _parity.check_case(w, causal, B=2, H=3, N=N, d=128, seed=N * 7 + 128, rows=rows,
+                       kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_pinned_n1k_full_tensor(kernel):
+    """The B1 H32 N1024 workload, every row of every head."""
+    w = W["n1k"]
+    rows = np.array([(bh, i) for bh in range(32) for i in range(1024)], dtype=np.int64)
+    _parity.check_case(w, True, rows=rows, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_pinned_large_logits(kernel):
+    _parity.check_case(W["n32k"], True, B=1, H=4, N=1000, d=128, seed=205, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("causal", [True, False])
+def test_pinned_many_units_per_cta(kernel, causal):
+    rows = workloads.select_rows(W["b8n8k"], B=4, H=40, N=1536, seed=6)
+    _parity.check_case(W["n1k"], causal, B=4, H=40, N=1536, d=128, seed=6, rows=rows,
+                       kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_pinned_long_sequence_sampled(kernel):
+    """One head at N = 16384: 128 (one-tile) or 64 (two-tile) units of very different
+    lengths under the causal mask."""
+    w = W["n32k"]
+    rows = workloads.select_rows(w, B=1, H=1, N=16384, seed=207)
+    _parity.check_case(w, True, B=1, H=1, N=16384, d=128, seed=207, rows=rows, kernel=kernel)
+
+
+def test_one_tile_grid_cap_and_determinism():
+    w = W["n1k"]
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w, B=2, H=8, N=1100, d=128, seed=12))
+    opt = fa.FwdOptions(kernel=ONE)
+    a, la = fa.fa_fwd(q, k, v, causal=True, options=opt)
+    b, lb = fa.fa_fwd(q, k, v, causal=True, options=fa.FwdOptions(kernel=ONE, max_ctas=7))
+    c, lc = fa.fa_fwd(q, k, v, causal=True, options=opt)
+    assert fa.get_device_status() == fa.FA_OK
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    assert torch.equal(a, c) and torch.equal(la, lc)
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 4, 8192), (1, 32, 1024), (2, 16, 4096)])
+def test_auto_equals_the_planned_kernel(B, H, N):
+    q, k, v = (t.cuda() for t in workloads.make_inputs(W["n4k"], B=B, H=H, N=N, d=128, seed=N))
+    kernel, splits = fa.fwd_plan(B, H, N, 128, True)
+    assert splits == 1
+    a, la = fa.fa_fwd(q, k, v, causal=True)
+    b, lb = fa.fa_fwd(q, k, v, causal=True, options=fa.FwdOptions(kernel=kernel))
+    assert fa.get_device_status() == fa.FA_OK
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_plan_uses_the_device_sm_count():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for H, N in [(1, 8192), (4, 8192), (1, 32768), (32, 8192)]:
+        for split in (False, True):
+            assert fa.fwd_plan(1, H, N, 128, True, allow_split=split) == \
+                fa.fwd_plan(1, H, N, 128, True, allow_split=split, num_sms=sms)
+
+
+@pytest.mark.parametrize("H,N", [(4, 8192), (1, 16384)])
+def test_automatic_split_entry_points(H, N):
+    """splits = 0 through both split entry points: the planned launch (one-tile at
+    H4 N8192, a four-way split at H1 N16384 on 152 SMs) against the oracle."""
+    w = W["n32k"]
+    q, k, v = workloads.make_inputs(w, B=1, H=H, N=N, d=128, seed=H + N)
+    rows = workloads.select_rows(w, B=1, H=H, N=N, seed=H + N)
+    scale = float(np.float32(1.0 / np.sqrt(128)))
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, True, scale)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    o, lse = fa.fa_fwd_splitkv(qd, kd, vd, causal=True, scale=scale, splits=0)
+    assert fa.get_device_status() == fa.FA_OK
+    _parity.compare(*_parity.gather_rows(o, lse, rows), o64, lse64)
+    o2 = torch.empty_like(qd)
+    lse2 = torch.empty((1, H, N), dtype=torch.float32, device="cuda")
+    rc = fa.fa_fwd_splitkv_noalloc_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o2.data_ptr(),
+                                       lse2.data_ptr(), 1, H, N, 128, True, scale, 0,
+                                       torch.cuda.current_stream().cuda_stream)
+    assert rc == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)

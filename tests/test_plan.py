@@ -1,0 +1,146 @@
+"""Host-side checks of the launch planner (fa_fwd_plan), no GPU needed.
+
+At head dim 128 the library chooses per call between the two-tile kernel (256-row
+units, optionally split along the keys) and the one-tile kernel (128-row units) by
+replaying the kernels' static schedule on a cost model.  These tests pin that choice
+to GB300 measurements: for every shape below one candidate was measured more than 2%
+faster than the others (d=128, bf16, mean of 20 launches; the table is the profile
+`kernel_choice_d128` under profiles/), and the planner, asked for 152 SMs, must pick
+it.  Near-ties (< 2%) are left out: either choice is right there.
+"""
+import ctypes
+
+import pytest
+
+import tiled_online_softmax_fa_gb300 as fa
+
+SMS = 152
+TWO, ONE = fa.FA_KERNEL_TWO_TILE, fa.FA_KERNEL_ONE_TILE
+
+# (B, H, N, causal) -> measured fastest of: "two" (two-tile unsplit), "one" (one-tile),
+# "split" (two-tile split as the split heuristic says; timed only where it splits)
+MEASURED = {
+    (1, 2, 16384, True): "one", (1, 4, 8192, True): "one", (1, 8, 4096, True): "one",
+    (1, 16, 2048, True): "one", (1, 32, 1024, True): "one", (1, 1, 65536, True): "two",
+    (1, 2, 32768, True): "two", (1, 4, 16384, True): "two", (1, 8, 8192, True): "two",
+    (1, 16, 4096, True): "two", (1, 32, 2048, True): "two", (1, 64, 1024, True): "one",
+    (1, 3, 16384, True): "one", (1, 6, 8192, True): "one", (1, 12, 4096, True): "one",
+    (1, 48, 1024, True): "one", (1, 1, 16384, True): "split", (1, 2, 8192, True): "one",
+    (1, 4, 4096, True): "one", (1, 16, 1024, True): "one", (1, 32, 512, True): "one",
+    (1, 32, 256, True): "one", (1, 20, 4096, True): "two", (1, 40, 2048, True): "two",
+    (1, 10, 8192, True): "two", (2, 16, 4096, True): "two", (1, 64, 2048, True): "two",
+    (1, 1, 24576, True): "split", (1, 3, 8192, True): "one", (1, 3, 12288, True): "one",
+    (1, 5, 6144, True): "one", (1, 6, 6144, True): "one", (1, 1, 12288, True): "one",
+    (1, 2, 24576, True): "one", (1, 32, 1024, False): "two", (1, 8, 4096, False): "two",
+    (1, 4, 8192, False): "two", (1, 32, 2048, False): "two", (1, 16, 4096, False): "two",
+    (1, 48, 2048, False): "two",
+}
+
+
+def _label(kernel, splits):
+    return "one" if kernel == ONE else ("split" if splits > 1 else "two")
+
+
+@pytest.mark.parametrize("shape,want", sorted(MEASURED.items()))
+def test_plan_picks_the_measured_fastest(shape, want):
+    B, H, N, causal = shape
+    kernel, splits = fa.fwd_plan(B, H, N, 128, causal, allow_split=True, num_sms=SMS)
+    assert _label(kernel, splits) == want
+    # without a workspace the split is not a candidate
+    kernel1, splits1 = fa.fwd_plan(B, H, N, 128, causal, allow_split=False, num_sms=SMS)
+    assert splits1 == 1
+    if want != "split":
+        assert _label(kernel1, splits1) == want
+
+
+def test_measured_two_vs_one_without_split():
+    # where the split won, the unsplit choice is between the other two: measured
+    # one-tile 489 vs two-tile 299 TFLOP/s (H1 N16384), 746 vs 452 (H1 N24576)
+    for N in (16384, 24576):
+        assert fa.fwd_plan(1, 1, N, 128, True, num_sms=SMS) == (ONE, 1)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_small_head_dims_take_the_two_tile_kernel(d):
+    for H, N in [(1, 1024), (4, 8192), (1, 32768), (32, 8192)]:
+        k, s = fa.fwd_plan(1, H, N, d, True, allow_split=True, num_sms=SMS)
+        assert k == TWO and s >= 1
+
+
+def test_head_dim_256_takes_the_one_tile_kernel_unsplit():
+    for H, N in [(1, 1024), (4, 8192), (1, 32768), (32, 8192)]:
+        assert fa.fwd_plan(1, H, N, 256, True, allow_split=True, num_sms=SMS) == (ONE, 1)
+
+
+def test_throughput_shape_takes_the_two_tile_kernel():
+    # B8 H32 N8192: 8192 units of 256 rows, far beyond the modelled range
+    assert fa.fwd_plan(8, 32, 8192, 128, True, allow_split=True, num_sms=SMS) == (TWO, 1)
+
+
+def test_many_units_skip_the_model():
+    # more than four 256-row units per SM: the two-tile kernel, whatever the mask
+    for causal in (True, False):
+        assert fa.fwd_plan(4, 160, 1024, 128, causal, num_sms=SMS)[0] == TWO
+
+
+def test_fewer_sms_shift_the_choice():
+    # 128 units of 256 rows: fewer than one per SM on 152 SMs (one-tile), but 16 per
+    # SM on 8 SMs, where the schedule is even and the faster two-tile step wins
+    assert fa.fwd_plan(1, 8, 4096, 128, True, num_sms=SMS)[0] == ONE
+    assert fa.fwd_plan(1, 8, 4096, 128, True, num_sms=8)[0] == TWO
+
+
+def test_batch_and_heads_enter_as_their_product():
+    for B, H in [(1, 8), (2, 4), (8, 1)]:
+        assert fa.fwd_plan(B, H, 4096, 128, True, num_sms=SMS) == (ONE, 1)
+
+
+def test_empty_problem():
+    assert fa.fwd_plan(0, 4, 128, 128, True, num_sms=SMS) == (TWO, 1)
+    assert fa.fwd_plan(1, 4, 0, 64, True, num_sms=SMS) == (TWO, 1)
+    assert fa.fwd_plan(1, 0, 128, 256, True, num_sms=SMS) == (ONE, 1)
+
+
+@pytest.mark.parametrize("args,want", [
+    ((-1, 1, 128, 128), fa.FA_ERR_INVALID_ARG),
+    ((1, 1, -128, 128), fa.FA_ERR_INVALID_ARG),
+    ((1, 1, 128, 48), fa.FA_ERR_UNSUPPORTED),
+    ((1, 1, (1 << 30) + 1, 128), fa.FA_ERR_UNSUPPORTED),
+])
+def test_plan_rejects_bad_sizes(args, want):
+    with pytest.raises(fa.FAError) as e:
+        fa.fwd_plan(*args, True, num_sms=SMS)
+    assert e.value.status == want
+
+
+def test_plan_rejects_null_outputs_and_negative_sms():
+    lib = fa.load_library()
+    k = ctypes.c_int()
+    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, SMS, None, ctypes.byref(k)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, SMS, ctypes.byref(k), None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, -1, ctypes.byref(k),
+                           ctypes.byref(ctypes.c_int())) == fa.FA_ERR_INVALID_ARG
+
+
+# --- the kernel pin in fa_fwd_options: checked before any CUDA call -------------------
+def _call_opts(d, **opt):
+    return fa.fa_fwd_raw(0x10000, 0x20000, 0x30000, 0x40000, 0, 1, 1, 128, d, True, 0.1,
+                         options=fa.FwdOptions(**opt))
+
+
+def test_options_struct_layout():
+    assert ctypes.sizeof(fa.FwdOptions) == 24
+    assert fa.FwdOptions.kernel.offset == 16 and fa.FwdOptions.reserved.offset == 20
+
+
+@pytest.mark.parametrize("d,opt,want", [
+    (128, dict(kernel=3), fa.FA_ERR_INVALID_ARG),
+    (128, dict(kernel=-1), fa.FA_ERR_INVALID_ARG),
+    (128, dict(reserved=1), fa.FA_ERR_INVALID_ARG),
+    (64, dict(kernel=ONE), fa.FA_ERR_UNSUPPORTED),
+    (16, dict(kernel=ONE), fa.FA_ERR_UNSUPPORTED),
+    (256, dict(kernel=TWO), fa.FA_ERR_UNSUPPORTED),
+])
+def test_kernel_pin_rejected_before_cuda(d, opt, want):
+    assert _call_opts(d, **opt) == want
+    assert fa.last_error()

@@ -29,13 +29,18 @@ FA_ERR_ARCH = 4
 FA_ERR_CUDA = 5
 FA_ERR_DEVICE_TIMEOUT = 6
 SUPPORTED_HEAD_DIMS = (16, 32, 64, 128, 256)
+FA_KERNEL_AUTO = 0
+FA_KERNEL_TWO_TILE = 1  # 256 query rows per work unit; head dims 16-128; split-KV
+FA_KERNEL_ONE_TILE = 2  # 128 query rows per work unit; head dims 128 and 256
 
 
 class FwdOptions(ctypes.Structure):
     """Mirror of ``fa_fwd_options``."""
     _fields_ = [("wait_budget_cycles", ctypes.c_int64),
                 ("inject_skip_kv_load", ctypes.c_int32),
-                ("max_ctas", ctypes.c_int32)]
+                ("max_ctas", ctypes.c_int32),
+                ("kernel", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class FAError(RuntimeError):
@@ -79,6 +84,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_int64
         lib.fa_splitkv_auto_splits.argtypes = [i64, i64, i64, ctypes.c_int]
         lib.fa_splitkv_auto_splits.restype = ctypes.c_int
+        lib.fa_fwd_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+        lib.fa_fwd_plan.restype = ctypes.c_int
         lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                                ctypes.c_int, ctypes.c_float, ctypes.c_int, vp]
         lib.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
@@ -169,6 +177,22 @@ def splitkv_auto_splits(B: int, H: int, N: int, causal: bool = True) -> int:
     return int(load_library().fa_splitkv_auto_splits(B, H, N, int(bool(causal))))
 
 
+def fwd_plan(B: int, H: int, N: int, d: int, causal: bool = True, allow_split: bool = False,
+             num_sms: int = 0) -> tuple[int, int]:
+    """(kernel, splits) the library picks for these sizes (fa_fwd_plan).
+
+    allow_split=False gives fa_fwd's choice, True that of fa_fwd_splitkv with splits=0.
+    num_sms=0 asks the current device; a positive count plans without touching CUDA.
+    """
+    kernel, splits = ctypes.c_int(), ctypes.c_int()
+    rc = load_library().fa_fwd_plan(int(B), int(H), int(N), int(d), int(bool(causal)),
+                                    int(bool(allow_split)), int(num_sms), ctypes.byref(kernel),
+                                    ctypes.byref(splits))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_plan")
+    return kernel.value, splits.value
+
+
 def fa_fwd_splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal, scale, splits,
                        ws_ptr, ws_bytes, stream: int = 0) -> int:
     """Call fa_fwd_splitkv with raw device addresses; returns the status code."""
@@ -194,8 +218,9 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, causal: bool = True, scale: float 
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    # head dim 256 has no split variant: the automatic choice there is one piece
-    use = splits if splits > 0 else (1 if d == 256 else splitkv_auto_splits(B, H, N, causal))
+    # splits = 0: the library plans the launch (kernel and pieces) itself; the workspace
+    # is sized for the pieces that plan takes
+    use = splits if splits > 0 else fwd_plan(B, H, N, d, causal, allow_split=True)[1]
     need = splitkv_workspace_bytes(B, H, N, d, use) if use > 1 else 0
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -206,7 +231,7 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, causal: bool = True, scale: float 
                 or not t.is_contiguous() or t.shape != q.shape:
             raise TypeError(f"{name} must be a contiguous CUDA bf16 tensor shaped like q")
     rc = fa_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), B, H, N, d, causal, scale, use, ws_ptr, ws_bytes,
+                            lse.data_ptr(), B, H, N, d, causal, scale, splits, ws_ptr, ws_bytes,
                             _stream_handle(stream, q.device))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_splitkv")

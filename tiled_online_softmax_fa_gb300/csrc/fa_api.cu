@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -26,7 +27,7 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 namespace {
 
-constexpr int kVersion = 100;  // 0.1.0
+constexpr int kVersion = 200;  // 0.2.0 (fa_fwd_options gained `kernel`)
 constexpr int kMaxDevices = 64;
 constexpr long long kDefaultBudget = 2000000000LL;  // ~1 s of SM clock
 
@@ -51,7 +52,8 @@ struct DeviceState {
   bool probed = false;
   bool arch_ok = false;
   int num_sms = 0;
-  bool smem_set[5] = {false, false, false, false, false};
+  bool smem_set[5] = {false, false, false, false, false};      // two-tile kernel, per head dim
+  bool smem_set_one[5] = {false, false, false, false, false};  // one-tile kernel
 };
 
 std::mutex g_mu;
@@ -153,6 +155,119 @@ bool workspace_fits(const void* ws, size_t size, int64_t BH, int64_t N, int64_t 
   return true;
 }
 
+// Heads per scheduling group: their K and V together take at most ~64 MB of L2.
+int64_t group_heads_for(int64_t BH, int64_t N, int64_t d) {
+  const int64_t kv_bytes_per_head = 2 * N * d * 2;
+  int64_t g = (int64_t{64} << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  return g;
+}
+
+// ---- kernel choice ------------------------------------------------------------------
+// At head dim 128 both kernels serve a call.  The two-tile kernel's 256-row units share
+// each K/V tile between two Q tiles and run a step ~1.2x faster; the one-tile kernel's
+// 128-row units are half as long, which matters when there are few units per SM: under
+// the causal mask unit lengths run from 1 to N/128 key tiles, and the longest units set
+// the finishing time.  The choice replays the static schedule both kernels follow
+// (unit_coords / unit_of: grouped longest-first order; in round k the CTA at grid
+// position c takes item k * grid + c, or k * grid + grid - 1 - c when k is odd) and
+// compares the busiest CTA's total.  Cost unit: one (128-row Q tile x 128-key tile) step
+// of the two-tile kernel.  The constants were fitted to GB300 timings at head dim 128
+// (82 kernel pairs over 44 shapes -- B 1-2, H 1-64, N 256-65536, causal and not -- and
+// 18 split-versus-one-tile pairs); with them the model picks the faster one in every
+// pair measured.
+constexpr double kTwoTileUnitCost = 1.0;   // fixed cost of an unsplit two-tile unit
+constexpr double kOneTileStepCost = 1.18;  // a one-tile kernel step, in two-tile steps
+constexpr double kSplitPieceCost = 6.0;    // fixed cost of one split piece
+constexpr double kMergeFixedCost = 5.0;    // the merge launch
+constexpr double kMergeCostPerMB = 1.0;    // per MB of fp32 partial outputs (written, merged)
+constexpr int kModelMaxSms = 1024;
+constexpr int64_t kModelUnitsPerSm = 4;      // more 256-row units per SM: two-tile kernel
+constexpr int64_t kModelMaxItems = 1 << 16;  // bound on the replayed schedule's length
+
+struct Plan {
+  int kernel;  // FA_KERNEL_TWO_TILE or FA_KERNEL_ONE_TILE
+  int splits;
+};
+
+// Key tiles a Q tile starting at row_start visits (the kernels' tiles_for).
+int64_t tiles_from(int64_t row_start, int64_t N, int64_t nkv, int causal) {
+  if (row_start >= N) return 0;
+  if (!causal) return nkv;
+  const int64_t t = row_start / fa_sm103::kBlockN + 1;
+  return t < nkv ? t : nkv;
+}
+
+// Query block (in units of `unit_rows`) of unit u in the grouped longest-first order.
+int64_t unit_block(int64_t u, int64_t BH, int64_t nqb, int64_t gh) {
+  const int64_t g = u / (gh * nqb);
+  const int64_t heads = std::min(gh, BH - g * gh);
+  return nqb - 1 - (u - g * gh * nqb) / heads;
+}
+
+// The busiest CTA's total cost when `items` items (costs cost(i), in launch order) are
+// handed out in the kernels' snake order over `grid` CTAs.
+template <class Cost>
+double snake_makespan(int64_t items, int grid, Cost cost) {
+  double load[kModelMaxSms] = {};
+  for (int64_t i = 0; i < items; ++i) {
+    const int64_t k = i / grid;
+    const int r = static_cast<int>(i - k * grid);
+    load[(k & 1) ? grid - 1 - r : r] += cost(i);
+  }
+  return *std::max_element(load, load + grid);
+}
+
+double model_two_tile(int64_t BH, int64_t N, int64_t d, int causal, int sms, int splits) {
+  const int64_t nqb = (N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows;
+  const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
+  const int64_t gh = group_heads_for(BH, N, d);
+  const int64_t items = nqb * BH * splits;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, items));
+  double t = snake_makespan(items, grid, [&](int64_t w) {
+    const int64_t u = w / splits, sp = w - u * splits;
+    const int64_t row0 = unit_block(u, BH, nqb, gh) * fa_sm103::kUnitRows;
+    const int64_t n0 = tiles_from(row0, N, nkv, causal);
+    const int64_t n1 = tiles_from(row0 + fa_sm103::kBlockM, N, nkv, causal);
+    const int64_t n = std::max(n0, n1);
+    const int64_t k0 = sp * n / splits, k1 = (sp + 1) * n / splits;
+    if (k1 <= k0) return 0.0;
+    const double steps = static_cast<double>(std::max<int64_t>(0, std::min(n0, k1) - k0) +
+                                             std::max<int64_t>(0, std::min(n1, k1) - k0));
+    return steps + (splits > 1 ? kSplitPieceCost : kTwoTileUnitCost);
+  });
+  if (splits > 1)
+    t += kMergeFixedCost + kMergeCostPerMB * static_cast<double>(splits * BH * N * d * 4) * 1e-6;
+  return t;
+}
+
+double model_one_tile(int64_t BH, int64_t N, int64_t d, int causal, int sms) {
+  const int64_t nqb = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1;
+  const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
+  const int64_t gh = group_heads_for(BH, N, d);
+  const int64_t items = nqb * BH;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, items));
+  return kOneTileStepCost * snake_makespan(items, grid, [&](int64_t u) {
+           const int64_t row0 = unit_block(u, BH, nqb, gh) * fa_sm103::one::kUnitRows1;
+           return static_cast<double>(tiles_from(row0, N, nkv, causal));
+         });
+}
+
+// The launch for a non-empty problem.  allow_split: the call has (or may size) a
+// workspace, so the two-tile kernel may split as choose_splits says.
+Plan plan_for(int64_t BH, int64_t N, int64_t d, int causal, int sms, bool allow_split) {
+  if (d == 256) return {FA_KERNEL_ONE_TILE, 1};
+  const int splits = allow_split ? choose_splits(BH, N, sms, causal) : 1;
+  const int64_t units = units_for(BH, N);
+  if (d != 128 || sms > kModelMaxSms || units > kModelUnitsPerSm * sms ||
+      units * splits > kModelMaxItems)
+    return {FA_KERNEL_TWO_TILE, splits};
+  const double two = model_two_tile(BH, N, d, causal, sms, splits);
+  const double one = model_one_tile(BH, N, d, causal, sms);
+  return one < two ? Plan{FA_KERNEL_ONE_TILE, 1} : Plan{FA_KERNEL_TWO_TILE, splits};
+}
+
 // Fields every launch shares.  `unit_rows` = query rows per work unit (256 for the
 // two-tile kernel, 128 for the head-dim-256 kernel).
 fa_sm103::Params base_params(void* o, float* lse, int64_t BH, int64_t N, int64_t d, int unit_rows,
@@ -169,12 +284,7 @@ fa_sm103::Params base_params(void* o, float* lse, int64_t BH, int64_t N, int64_t
   p.num_items = p.num_units;
   p.ws_o = nullptr;
   p.ws_lse = nullptr;
-  // heads per scheduling group: their K and V together take at most ~64 MB of L2
-  const int64_t kv_bytes_per_head = 2 * N * d * 2;
-  int64_t g = (int64_t{64} << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
-  if (g < 1) g = 1;
-  if (g > BH) g = BH;
-  p.group_heads = static_cast<int>(g);
+  p.group_heads = static_cast<int>(group_heads_for(BH, N, d));
   p.causal = causal ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.budget = (opts && opts->wait_budget_cycles > 0) ? opts->wait_budget_cycles : kDefaultBudget;
@@ -233,11 +343,11 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   return FA_OK;
 }
 
-// Head dim 256: the one-Q-tile kernel (128-row units, no split-KV variant).
-int launch_d256(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
-                int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
-                bool& smem_set, const fa_fwd_options* opts) {
-  constexpr int HD = 256;
+// The one-Q-tile kernel (128-row units, no split-KV variant): head dims 256 and 128.
+template <int HD>
+int launch_one(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
+               int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
+               bool& smem_set, const fa_fwd_options* opts) {
   constexpr int SMEM = fa_sm103::one::Cfg1<HD>::SMEM_BYTES;
   CUtensorMap mq, mk, mv;
   int st;
@@ -294,11 +404,14 @@ int device_state(DeviceState** out) {
 
 namespace {
 
-// Shared body of every forward entry point.  splits = 0 chooses a split count (only
-// used when workspace is non-null); splits = 1 is the unsplit kernel.
+// Shared body of every forward entry point.  splits = 0 lets plan_for choose the kernel
+// and the split count (a split needs the workspace); splits = 1 runs unsplit on the
+// kernel plan_for picks without splits, or on `kernel` when that is not FA_KERNEL_AUTO;
+// splits > 1 runs the two-tile kernel split that many ways.
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
             int64_t H, int64_t N, int64_t d, int causal, float scale, void* stream,
-            const fa_fwd_options* opts, int splits, void* workspace, size_t workspace_size) {
+            const fa_fwd_options* opts, int splits, void* workspace, size_t workspace_size,
+            int kernel = FA_KERNEL_AUTO) {
   t_last_error.clear();
   // ---- pure argument checks: no CUDA call before these pass ----
   if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
@@ -311,7 +424,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (B > INT32_MAX / H) return set_error(FA_ERR_UNSUPPORTED, "B*H too large");
   const int64_t BH = B * H;
   if (N > (int64_t{1} << 30)) return set_error(FA_ERR_UNSUPPORTED, "N too large");
-  const int64_t unit_rows = d == 256 ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
+  // head dims 128 and 256 may run the one-tile kernel's 128-row units
+  const int64_t unit_rows = d >= 128 ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
   const int64_t units = ((N + unit_rows - 1) / unit_rows) * BH;
   if (units > INT32_MAX) return set_error(FA_ERR_UNSUPPORTED, "too many work units");
   if (BH > (INT64_MAX / 4) / (N * d)) return set_error(FA_ERR_UNSUPPORTED, "tensor too large");
@@ -330,6 +444,15 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (lse && overlaps(lse, lse_bytes, o, bytes)) return set_error(FA_ERR_INVALID_ARG, "lse overlaps o");
   if (opts && (opts->wait_budget_cycles < 0 || opts->inject_skip_kv_load < 0 || opts->max_ctas < 0))
     return set_error(FA_ERR_INVALID_ARG, "negative option");
+  if (opts && opts->reserved != 0) return set_error(FA_ERR_INVALID_ARG, "reserved option not 0");
+  if (kernel < FA_KERNEL_AUTO || kernel > FA_KERNEL_ONE_TILE)
+    return set_error(FA_ERR_INVALID_ARG, "unknown kernel");
+  if (kernel == FA_KERNEL_TWO_TILE && d == 256)
+    return set_error(FA_ERR_UNSUPPORTED, "the two-tile kernel serves head dims 16 to 128");
+  if (kernel == FA_KERNEL_ONE_TILE && d != 128 && d != 256)
+    return set_error(FA_ERR_UNSUPPORTED, "the one-tile kernel serves head dims 128 and 256");
+  if (kernel != FA_KERNEL_AUTO && splits != 1)
+    return set_error(FA_ERR_INVALID_ARG, "a pinned kernel runs unsplit");
   if (splits < 0 || splits > kMaxSplits)
     return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
   if (d == 256) {
@@ -351,19 +474,28 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (st != FA_OK) return st;
   if (!dev->arch_ok) return set_error(FA_ERR_ARCH, "device is not sm_103 (GB300-class)");
   if (splits == 0) {
-    splits = choose_splits(BH, N, dev->num_sms, causal);
+    const Plan pl = plan_for(BH, N, d, causal, dev->num_sms, true);
+    kernel = pl.kernel;
+    splits = pl.splits;
     if (splits > 1 && !workspace_fits(workspace, workspace_size, BH, N, d, splits, q, k, v, o,
                                       bytes, lse, lse_bytes))
       return FA_ERR_INVALID_ARG;
+  } else if (kernel == FA_KERNEL_AUTO) {
+    kernel = splits == 1 ? plan_for(BH, N, d, causal, dev->num_sms, false).kernel
+                         : static_cast<int>(FA_KERNEL_TWO_TILE);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kernel == FA_KERNEL_ONE_TILE) {
+    bool& set_one = dev->smem_set_one[hd];
+    return d == 256 ? launch_one<256>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts)
+                    : launch_one<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
+  }
   bool& smem_set = dev->smem_set[hd];
   switch (hd) {
     case 0: return launch<16>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
     case 1: return launch<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
     case 2: return launch<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
-    case 3: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
-    default: return launch_d256(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts);
+    default: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
   }
 }
 
@@ -374,7 +506,8 @@ extern "C" {
 int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                 int64_t H, int64_t N, int64_t d, int causal, float scale, void* stream,
                 const fa_fwd_options* opts) {
-  return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, opts, 1, nullptr, 0);
+  return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, opts, 1, nullptr, 0,
+                 opts ? opts->kernel : FA_KERNEL_AUTO);
 }
 
 int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits) {
@@ -390,6 +523,32 @@ int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal) {
   DeviceState* dev = nullptr;
   if (device_state(&dev) != FA_OK) return 1;
   return choose_splits(B * H, N, dev->num_sms, causal);
+}
+
+int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allow_split,
+                int num_sms, int* kernel, int* splits) {
+  t_last_error.clear();
+  if (!kernel || !splits) return set_error(FA_ERR_INVALID_ARG, "null output pointer");
+  if (B < 0 || H < 0 || N < 0 || num_sms < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
+  if (head_dim_index(d) < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64, 128 or 256");
+  if (B == 0 || H == 0 || N == 0) {
+    *kernel = d == 256 ? FA_KERNEL_ONE_TILE : FA_KERNEL_TWO_TILE;
+    *splits = 1;
+    return FA_OK;
+  }
+  if (B > INT32_MAX / H || N > (int64_t{1} << 30))
+    return set_error(FA_ERR_UNSUPPORTED, "sizes beyond the kernel's range");
+  int sms = num_sms;
+  if (sms == 0) {
+    DeviceState* dev = nullptr;
+    const int st = device_state(&dev);
+    if (st != FA_OK) return st;
+    sms = dev->num_sms;
+  }
+  const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, sms, allow_split != 0);
+  *kernel = pl.kernel;
+  *splits = pl.splits;
+  return FA_OK;
 }
 
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
@@ -450,7 +609,12 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   DeviceState* dev = nullptr;
   int st = device_state(&dev);
   if (st != FA_OK) return st;
-  if (splits == 0) splits = d == 256 ? 1 : choose_splits(B * H, N, dev->num_sms, causal);
+  int kernel = FA_KERNEL_AUTO;
+  if (splits == 0) {
+    const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, dev->num_sms, true);
+    kernel = pl.kernel;
+    splits = pl.splits;
+  }
   const int64_t need = workspace_bytes(B * H, N, d, splits);
   if (need > static_cast<int64_t>(kStaticScratchBytes)) {
     char buf[200];
@@ -463,7 +627,7 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   void* scratch = nullptr;
   if (splits > 1 && (st = static_scratch_address(&scratch)) != FA_OK) return st;
   return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, nullptr, splits, scratch,
-                 splits > 1 ? kStaticScratchBytes : 0);
+                 splits > 1 ? kStaticScratchBytes : 0, splits == 1 ? kernel : FA_KERNEL_AUTO);
 }
 
 int64_t fa_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kStaticScratchBytes); }
