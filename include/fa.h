@@ -51,8 +51,9 @@ typedef enum {
  *   B, H, N  batch, heads, sequence length (queries = keys = N).  B*H*N == 0 is a no-op.
  *   d        head dimension, one of 16, 32, 64, 128, 256.  (256 runs a kernel with one
  *            128-row query tile per work unit: 2 x 128 score columns + 256 output
- *            columns fill the 512 tensor-memory columns of an SM.  At 128 the library
- *            picks that kernel or the two-tile one per call; see fa_fwd_plan.)
+ *            columns fill the 512 tensor-memory columns of an SM.  At 32, 64 and 128
+ *            the library picks that kernel or the two-tile one per call; see
+ *            fa_fwd_plan.)
  *   causal   nonzero: query i attends keys j <= i (top-left aligned square mask).
  *   scale    finite, >= 0 (usually 1/sqrt(d)); applied to q.k before the softmax.
  *   stream   cudaStream_t to launch on (NULL = the legacy default stream).
@@ -100,7 +101,7 @@ typedef enum {
     FA_KERNEL_AUTO = 0,
     FA_KERNEL_TWO_TILE = 1,  /* 256 query rows per unit (two 128-row Q tiles sharing each
                                 K/V tile); head dims 16-128; the only one with split-KV */
-    FA_KERNEL_ONE_TILE = 2   /* 128 query rows per unit; head dims 128 and 256 */
+    FA_KERNEL_ONE_TILE = 2   /* 128 query rows per unit; head dims 32 to 256 */
 } fa_kernel;
 
 /* fa_fwd with options; opts may be NULL (same as fa_fwd). */
@@ -153,14 +154,14 @@ int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
  * the current device for its SM count (a CUDA call); > 0 plans for that many SMs
  * without touching CUDA.
  *
- * Head dims 16-64 always take the two-tile kernel and 256 the one-tile kernel.  At 128,
- * when there are at most four 256-row units per SM, the library models the run time of
- * each candidate -- the two-tile kernel unsplit, split as fa_splitkv_auto_splits says,
- * and the one-tile kernel -- by replaying the kernels' static schedule (unit lengths in
- * key tiles; a one-tile kernel tile costing 1.18 two-tile tiles; fixed costs of 1 tile
- * per unsplit two-tile unit and 6 per split piece; the merge 5 tiles plus 1 per MB of
- * partial results; all fitted to GB300 timings) and takes the shortest.  Few long units (one head at N = 8192) go
- * to the one-tile kernel, whose half-size units spread the causal triangle more evenly.
+ * Head dim 16 always takes the two-tile kernel and 256 the one-tile kernel.  At 32, 64
+ * and 128, when there are at most four 256-row units per SM, the library models the run
+ * time of each candidate -- the two-tile kernel unsplit, split as fa_splitkv_auto_splits
+ * says, and the one-tile kernel -- by replaying the kernels' static schedule (unit
+ * lengths in key tiles, a one-tile step costing 1.14-1.18 two-tile steps, fixed costs
+ * per unit, per split piece and for the merge, all fitted per head dim to GB300 timings)
+ * and takes the shortest.  Few long units (one head at N = 8192) go to the one-tile
+ * kernel, whose half-size units spread the causal triangle more evenly.
  *
  * Returns FA_OK, FA_ERR_INVALID_ARG (negative size, null output pointer) or
  * FA_ERR_UNSUPPORTED (head dim); an empty problem plans (FA_KERNEL_TWO_TILE, 1), or

@@ -1,7 +1,7 @@
-"""GPU parity of both head-dim-128 kernels and of the launch the planner picks.
+"""GPU parity of both kernels at head dims 32-128 and of the launch the planner picks.
 
-At head dim 128 a call runs either the two-tile kernel (256-row units) or the
-one-tile kernel (128-row units), whichever fa_fwd_plan models as faster; small
+At head dims 32, 64 and 128 a call runs either the two-tile kernel (256-row units) or
+the one-tile kernel (128-row units), whichever fa_fwd_plan models as faster; small
 problems go to the one-tile kernel.  Each kernel is pinned here through
 fa_fwd_options.kernel and compared with the fp64 oracle on the same seeded inputs,
 so both stay covered whatever the planner picks for the other tests' shapes.
@@ -80,10 +80,11 @@ def test_one_tile_grid_cap_and_determinism():
     assert torch.equal(a, c) and torch.equal(la, lc)
 
 
+@pytest.mark.parametrize("d", [128, 64, 32])
 @pytest.mark.parametrize("B,H,N", [(1, 4, 8192), (1, 32, 1024), (2, 16, 4096)])
-def test_auto_equals_the_planned_kernel(B, H, N):
-    q, k, v = (t.cuda() for t in workloads.make_inputs(W["n4k"], B=B, H=H, N=N, d=128, seed=N))
-    kernel, splits = fa.fwd_plan(B, H, N, 128, True)
+def test_auto_equals_the_planned_kernel(d, B, H, N):
+    q, k, v = (t.cuda() for t in workloads.make_inputs(W["n4k"], B=B, H=H, N=N, d=d, seed=N))
+    kernel, splits = fa.fwd_plan(B, H, N, d, True)
     assert splits == 1
     a, la = fa.fa_fwd(q, k, v, causal=True)
     b, lb = fa.fa_fwd(q, k, v, causal=True, options=fa.FwdOptions(kernel=kernel))
@@ -121,3 +122,21 @@ def test_automatic_split_entry_points(H, N):
     torch.cuda.synchronize()
     assert fa.get_device_status() == fa.FA_OK
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 257, 700])
+@pytest.mark.parametrize("causal", [True, False])
+def test_pinned_one_tile_small_head_dims(d, N, causal):
+    """The one-tile kernel at head dims 32 and 64 (each output row written by two
+    threads in 32-column chunks; at d = 32 the second thread writes none)."""
+    w = W["n1k"]
+    rows = workloads.select_rows(w, B=2, H=3, N=N, seed=N + d)
+    _parity.check_case(w, causal, B=2, H=3, N=N, d=d, seed=N * 5 + d, rows=rows, kernel=ONE)
+
+
+@pytest.mark.parametrize("d", [32, 64])
+def test_pinned_one_tile_small_head_dims_large_logits_and_many_units(d):
+    _parity.check_case(W["n32k"], True, B=1, H=4, N=1000, d=d, seed=300 + d, kernel=ONE)
+    rows = workloads.select_rows(W["b8n8k"], B=4, H=40, N=1536, seed=d)
+    _parity.check_case(W["n1k"], True, B=4, H=40, N=1536, d=d, seed=d, rows=rows, kernel=ONE)

@@ -1,12 +1,12 @@
 """Host-side checks of the launch planner (fa_fwd_plan), no GPU needed.
 
-At head dim 128 the library chooses per call between the two-tile kernel (256-row
-units, optionally split along the keys) and the one-tile kernel (128-row units) by
-replaying the kernels' static schedule on a cost model.  These tests pin that choice
+At head dims 32, 64 and 128 the library chooses per call between the two-tile kernel
+(256-row units, optionally split along the keys) and the one-tile kernel (128-row
+units) by replaying the kernels' static schedule on a cost model.  These tests pin that choice
 to GB300 measurements: for every shape below one candidate was measured more than 2%
-faster than the others (d=128, bf16, mean of 20 launches; the table is the profile
-`kernel_choice_d128` under profiles/), and the planner, asked for 152 SMs, must pick
-it.  Near-ties (< 2%) are left out: either choice is right there.
+faster than the others (bf16, mean of 20 launches; the tables are the profiles
+`kernel_choice_d128` and `kernel_choice_d64_d32` under profiles/), and the planner,
+asked for 152 SMs, must pick it.  Near-ties (< 2%) are left out: either choice is right there.
 """
 import ctypes
 
@@ -37,17 +37,53 @@ MEASURED = {
 }
 
 
+# the same at head dims 64 and 32 (profile `kernel_choice_d64_d32`)
+MEASURED_D64 = {
+    (1, 2, 16384, True): "one", (1, 4, 8192, True): "one", (1, 8, 4096, True): "one",
+    (1, 16, 2048, True): "one", (1, 32, 1024, True): "one", (1, 1, 65536, True): "two",
+    (1, 2, 32768, True): "two", (1, 4, 16384, True): "two", (1, 8, 8192, True): "two",
+    (1, 16, 4096, True): "two", (1, 32, 2048, True): "one", (1, 64, 1024, True): "one",
+    (1, 3, 16384, True): "one", (1, 6, 8192, True): "one", (1, 12, 4096, True): "one",
+    (1, 24, 2048, True): "one", (1, 48, 1024, True): "one", (1, 1, 16384, True): "split",
+    (1, 2, 8192, True): "one", (1, 4, 4096, True): "one", (1, 16, 1024, True): "one",
+    (1, 32, 512, True): "one", (1, 32, 256, True): "one", (1, 20, 4096, True): "two",
+    (1, 10, 8192, True): "two", (2, 16, 4096, True): "two", (1, 48, 2048, True): "one",
+    (1, 1, 24576, True): "split", (1, 2, 12288, True): "one", (1, 3, 8192, True): "one",
+    (1, 3, 12288, True): "one", (1, 5, 6144, True): "one", (1, 6, 6144, True): "one",
+    (1, 1, 12288, True): "one", (1, 2, 24576, True): "one", (1, 32, 1024, False): "two",
+    (1, 8, 4096, False): "two", (1, 4, 8192, False): "two", (1, 32, 2048, False): "two",
+    (1, 16, 4096, False): "two", (1, 48, 2048, False): "two",
+}
+MEASURED_D32 = {
+    (1, 2, 16384, True): "one", (1, 4, 8192, True): "one", (1, 8, 4096, True): "one",
+    (1, 16, 2048, True): "one", (1, 32, 1024, True): "one", (1, 1, 65536, True): "two",
+    (1, 2, 32768, True): "two", (1, 4, 16384, True): "two", (1, 8, 8192, True): "two",
+    (1, 16, 4096, True): "two", (1, 64, 1024, True): "one", (1, 3, 16384, True): "one",
+    (1, 6, 8192, True): "one", (1, 12, 4096, True): "one", (1, 24, 2048, True): "one",
+    (1, 1, 16384, True): "split", (1, 2, 8192, True): "one", (1, 4, 4096, True): "one",
+    (1, 16, 1024, True): "one", (1, 32, 512, True): "one", (1, 32, 256, True): "one",
+    (1, 20, 4096, True): "two", (1, 10, 8192, True): "two", (2, 16, 4096, True): "two",
+    (1, 48, 2048, True): "one", (1, 1, 24576, True): "split", (1, 2, 12288, True): "one",
+    (1, 3, 8192, True): "one", (1, 3, 12288, True): "one", (1, 5, 6144, True): "one",
+    (1, 6, 6144, True): "one", (1, 1, 12288, True): "one", (1, 2, 24576, True): "one",
+    (1, 32, 1024, False): "two", (1, 8, 4096, False): "two", (1, 4, 8192, False): "two",
+    (1, 32, 2048, False): "two", (1, 16, 4096, False): "two", (1, 48, 2048, False): "two",
+}
+
+
 def _label(kernel, splits):
     return "one" if kernel == ONE else ("split" if splits > 1 else "two")
 
 
-@pytest.mark.parametrize("shape,want", sorted(MEASURED.items()))
-def test_plan_picks_the_measured_fastest(shape, want):
+@pytest.mark.parametrize("d,shape,want", [(128, k, w) for k, w in sorted(MEASURED.items())] +
+                         [(64, k, w) for k, w in sorted(MEASURED_D64.items())] +
+                         [(32, k, w) for k, w in sorted(MEASURED_D32.items())])
+def test_plan_picks_the_measured_fastest(d, shape, want):
     B, H, N, causal = shape
-    kernel, splits = fa.fwd_plan(B, H, N, 128, causal, allow_split=True, num_sms=SMS)
+    kernel, splits = fa.fwd_plan(B, H, N, d, causal, allow_split=True, num_sms=SMS)
     assert _label(kernel, splits) == want
     # without a workspace the split is not a candidate
-    kernel1, splits1 = fa.fwd_plan(B, H, N, 128, causal, allow_split=False, num_sms=SMS)
+    kernel1, splits1 = fa.fwd_plan(B, H, N, d, causal, allow_split=False, num_sms=SMS)
     assert splits1 == 1
     if want != "split":
         assert _label(kernel1, splits1) == want
@@ -60,10 +96,10 @@ def test_measured_two_vs_one_without_split():
         assert fa.fwd_plan(1, 1, N, 128, True, num_sms=SMS) == (ONE, 1)
 
 
-@pytest.mark.parametrize("d", [16, 32, 64])
-def test_small_head_dims_take_the_two_tile_kernel(d):
+def test_head_dim_16_takes_the_two_tile_kernel():
+    # the one-tile kernel writes each output row in 32-column chunks: head dim >= 32
     for H, N in [(1, 1024), (4, 8192), (1, 32768), (32, 8192)]:
-        k, s = fa.fwd_plan(1, H, N, d, True, allow_split=True, num_sms=SMS)
+        k, s = fa.fwd_plan(1, H, N, 16, True, allow_split=True, num_sms=SMS)
         assert k == TWO and s >= 1
 
 
@@ -137,7 +173,6 @@ def test_options_struct_layout():
     (128, dict(kernel=3), fa.FA_ERR_INVALID_ARG),
     (128, dict(kernel=-1), fa.FA_ERR_INVALID_ARG),
     (128, dict(reserved=1), fa.FA_ERR_INVALID_ARG),
-    (64, dict(kernel=ONE), fa.FA_ERR_UNSUPPORTED),
     (16, dict(kernel=ONE), fa.FA_ERR_UNSUPPORTED),
     (256, dict(kernel=TWO), fa.FA_ERR_UNSUPPORTED),
 ])

@@ -31,7 +31,7 @@ FA_ERR_DEVICE_TIMEOUT = 6
 SUPPORTED_HEAD_DIMS = (16, 32, 64, 128, 256)
 FA_KERNEL_AUTO = 0
 FA_KERNEL_TWO_TILE = 1  # 256 query rows per work unit; head dims 16-128; split-KV
-FA_KERNEL_ONE_TILE = 2  # 128 query rows per work unit; head dims 128 and 256
+FA_KERNEL_ONE_TILE = 2  # 128 query rows per work unit; head dims 32 to 256
 
 
 class FwdOptions(ctypes.Structure):

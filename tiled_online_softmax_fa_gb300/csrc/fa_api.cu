@@ -165,26 +165,39 @@ int64_t group_heads_for(int64_t BH, int64_t N, int64_t d) {
 }
 
 // ---- kernel choice ------------------------------------------------------------------
-// At head dim 128 both kernels serve a call.  The two-tile kernel's 256-row units share
-// each K/V tile between two Q tiles and run a step ~1.2x faster; the one-tile kernel's
-// 128-row units are half as long, which matters when there are few units per SM: under
-// the causal mask unit lengths run from 1 to N/128 key tiles, and the longest units set
-// the finishing time.  The choice replays the static schedule both kernels follow
-// (unit_coords / unit_of: grouped longest-first order; in round k the CTA at grid
+// At head dims 32 to 128 both kernels serve a call.  The two-tile kernel's 256-row units
+// share each K/V tile between two Q tiles and run a step 1.14-1.18x faster; the one-tile
+// kernel's 128-row units are half as long, which matters when there are few units per
+// SM: under the causal mask unit lengths run from 1 to N/128 key tiles, and the longest
+// units set the finishing time.  The choice replays the static schedule both kernels
+// follow (unit_coords / unit_of: grouped longest-first order; in round k the CTA at grid
 // position c takes item k * grid + c, or k * grid + grid - 1 - c when k is odd) and
 // compares the busiest CTA's total.  Cost unit: one (128-row Q tile x 128-key tile) step
-// of the two-tile kernel.  The constants were fitted to GB300 timings at head dim 128
-// (82 kernel pairs over 44 shapes -- B 1-2, H 1-64, N 256-65536, causal and not -- and
-// 18 split-versus-one-tile pairs); with them the model picks the faster one in every
-// pair measured.
-constexpr double kTwoTileUnitCost = 1.0;   // fixed cost of an unsplit two-tile unit
-constexpr double kOneTileStepCost = 1.18;  // a one-tile kernel step, in two-tile steps
-constexpr double kSplitPieceCost = 6.0;    // fixed cost of one split piece
-constexpr double kMergeFixedCost = 5.0;    // the merge launch
-constexpr double kMergeCostPerMB = 1.0;    // per MB of fp32 partial outputs (written, merged)
+// of the two-tile kernel.
+struct CostModel {
+  double two_unit;      // fixed cost of an unsplit two-tile unit
+  double one_unit;      // fixed cost of a one-tile unit, in one-tile steps
+  double one_step;      // a one-tile kernel step, in two-tile steps
+  double split_piece;   // fixed cost of one split piece
+  double merge_fixed;   // the merge launch
+  double merge_per_mb;  // per MB of fp32 partial outputs (written, merged)
+};
+// Fitted to GB300 timings: at d = 128, 82 two-vs-one pairs over 44 shapes (B 1-2, H 1-64,
+// N 256-65536, causal and not) and 18 split-vs-one-tile pairs; at d = 64 and 32, 88
+// two-vs-one pairs over the same shapes and 20 split-vs-one-tile pairs.  With them the
+// model picks the faster launch in every pair measured but one near-tie (0.4 %).
+constexpr CostModel kCostD128 = {1.0, 0.0, 1.18, 6.0, 5.0, 1.0};
+constexpr CostModel kCostD32To64 = {4.0, 1.0, 1.14, 12.0, 30.0, 0.5};
 constexpr int kModelMaxSms = 1024;
 constexpr int64_t kModelUnitsPerSm = 4;      // more 256-row units per SM: two-tile kernel
 constexpr int64_t kModelMaxItems = 1 << 16;  // bound on the replayed schedule's length
+
+// The cost table of a head dim both kernels serve, else null.
+const CostModel* cost_model(int64_t d) {
+  if (d == 128) return &kCostD128;
+  if (d == 32 || d == 64) return &kCostD32To64;
+  return nullptr;
+}
 
 struct Plan {
   int kernel;  // FA_KERNEL_TWO_TILE or FA_KERNEL_ONE_TILE
@@ -219,7 +232,8 @@ double snake_makespan(int64_t items, int grid, Cost cost) {
   return *std::max_element(load, load + grid);
 }
 
-double model_two_tile(int64_t BH, int64_t N, int64_t d, int causal, int sms, int splits) {
+double model_two_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int causal, int sms,
+                      int splits) {
   const int64_t nqb = (N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows;
   const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
   const int64_t gh = group_heads_for(BH, N, d);
@@ -235,22 +249,22 @@ double model_two_tile(int64_t BH, int64_t N, int64_t d, int causal, int sms, int
     if (k1 <= k0) return 0.0;
     const double steps = static_cast<double>(std::max<int64_t>(0, std::min(n0, k1) - k0) +
                                              std::max<int64_t>(0, std::min(n1, k1) - k0));
-    return steps + (splits > 1 ? kSplitPieceCost : kTwoTileUnitCost);
+    return steps + (splits > 1 ? cm.split_piece : cm.two_unit);
   });
   if (splits > 1)
-    t += kMergeFixedCost + kMergeCostPerMB * static_cast<double>(splits * BH * N * d * 4) * 1e-6;
+    t += cm.merge_fixed + cm.merge_per_mb * static_cast<double>(splits * BH * N * d * 4) * 1e-6;
   return t;
 }
 
-double model_one_tile(int64_t BH, int64_t N, int64_t d, int causal, int sms) {
+double model_one_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int causal, int sms) {
   const int64_t nqb = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1;
   const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
   const int64_t gh = group_heads_for(BH, N, d);
   const int64_t items = nqb * BH;
   const int grid = static_cast<int>(std::min<int64_t>(sms, items));
-  return kOneTileStepCost * snake_makespan(items, grid, [&](int64_t u) {
+  return cm.one_step * snake_makespan(items, grid, [&](int64_t u) {
            const int64_t row0 = unit_block(u, BH, nqb, gh) * fa_sm103::one::kUnitRows1;
-           return static_cast<double>(tiles_from(row0, N, nkv, causal));
+           return static_cast<double>(tiles_from(row0, N, nkv, causal)) + cm.one_unit;
          });
 }
 
@@ -260,11 +274,12 @@ Plan plan_for(int64_t BH, int64_t N, int64_t d, int causal, int sms, bool allow_
   if (d == 256) return {FA_KERNEL_ONE_TILE, 1};
   const int splits = allow_split ? choose_splits(BH, N, sms, causal) : 1;
   const int64_t units = units_for(BH, N);
-  if (d != 128 || sms > kModelMaxSms || units > kModelUnitsPerSm * sms ||
+  const CostModel* cm = cost_model(d);
+  if (!cm || sms > kModelMaxSms || units > kModelUnitsPerSm * sms ||
       units * splits > kModelMaxItems)
     return {FA_KERNEL_TWO_TILE, splits};
-  const double two = model_two_tile(BH, N, d, causal, sms, splits);
-  const double one = model_one_tile(BH, N, d, causal, sms);
+  const double two = model_two_tile(*cm, BH, N, d, causal, sms, splits);
+  const double one = model_one_tile(*cm, BH, N, d, causal, sms);
   return one < two ? Plan{FA_KERNEL_ONE_TILE, 1} : Plan{FA_KERNEL_TWO_TILE, splits};
 }
 
@@ -424,8 +439,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (B > INT32_MAX / H) return set_error(FA_ERR_UNSUPPORTED, "B*H too large");
   const int64_t BH = B * H;
   if (N > (int64_t{1} << 30)) return set_error(FA_ERR_UNSUPPORTED, "N too large");
-  // head dims 128 and 256 may run the one-tile kernel's 128-row units
-  const int64_t unit_rows = d >= 128 ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
+  // head dims 32 to 256 may run the one-tile kernel's 128-row units
+  const int64_t unit_rows = d >= 32 ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
   const int64_t units = ((N + unit_rows - 1) / unit_rows) * BH;
   if (units > INT32_MAX) return set_error(FA_ERR_UNSUPPORTED, "too many work units");
   if (BH > (INT64_MAX / 4) / (N * d)) return set_error(FA_ERR_UNSUPPORTED, "tensor too large");
@@ -449,8 +464,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
     return set_error(FA_ERR_INVALID_ARG, "unknown kernel");
   if (kernel == FA_KERNEL_TWO_TILE && d == 256)
     return set_error(FA_ERR_UNSUPPORTED, "the two-tile kernel serves head dims 16 to 128");
-  if (kernel == FA_KERNEL_ONE_TILE && d != 128 && d != 256)
-    return set_error(FA_ERR_UNSUPPORTED, "the one-tile kernel serves head dims 128 and 256");
+  if (kernel == FA_KERNEL_ONE_TILE && d < 32)
+    return set_error(FA_ERR_UNSUPPORTED, "the one-tile kernel serves head dims 32 to 256");
   if (kernel != FA_KERNEL_AUTO && splits != 1)
     return set_error(FA_ERR_INVALID_ARG, "a pinned kernel runs unsplit");
   if (splits < 0 || splits > kMaxSplits)
@@ -487,8 +502,12 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kernel == FA_KERNEL_ONE_TILE) {
     bool& set_one = dev->smem_set_one[hd];
-    return d == 256 ? launch_one<256>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts)
-                    : launch_one<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
+    switch (hd) {
+      case 1: return launch_one<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
+      case 2: return launch_one<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
+      case 3: return launch_one<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
+      default: return launch_one<256>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
+    }
   }
   bool& smem_set = dev->smem_set[hd];
   switch (hd) {

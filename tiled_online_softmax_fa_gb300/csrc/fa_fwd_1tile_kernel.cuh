@@ -1,4 +1,4 @@
-// fa_fwd_1tile_kernel.cuh -- the one-Q-tile attention forward kernel (head dims 256 and 128).
+// fa_fwd_1tile_kernel.cuh -- the one-Q-tile attention forward kernel (head dims 32 to 256).
 //
 // Same method and numerics as fa_fwd_kernel (blocked online softmax of the aiml.sh
 // "Speed up long contexts with FlashAttention" lab.py `tiled_flash_attention`, lazy
@@ -6,8 +6,8 @@
 //   * Tensor memory (512 columns): S buffer 0 | S buffer 1 | O (HD fp32 columns).
 //     At head dim 256 two 128-row Q tiles (the other kernel's unit) would need 768
 //     columns, so a work unit here is one (batch*head, 128-query-row tile).  At head
-//     dim 128 the same half-size unit serves launches with too few 256-row units to
-//     fill the SMs evenly (the host picks the kernel from a schedule model).
+//     dims 32 to 128 the same half-size unit serves launches with too few 256-row
+//     units to fill the SMs evenly (the host picks the kernel from a schedule model).
 //   * The two S buffers let S(j+1) be computed while the softmax works on S(j): MMA
 //     order S(0), S(1), then for each KV tile j: PV(j), S(j+2).  P(j) is written over
 //     S buffer j % 2; S(j+2) reuses it only after PV(j) (MMAs of one thread run in
@@ -15,7 +15,8 @@
 //   * Shared memory, filled by TMA with the 128-byte swizzle: at head dim 256 one
 //     64 KB Q tile and a 2-slot ring of 64 KB K/V tiles; at head dim 128 two 32 KB Q
 //     buffers (the next unit's Q loads during this one) and a 4-slot ring of 32 KB
-//     K/V tiles.  Both take 192 KB + 1 KB alignment.
+//     K/V tiles (both 192 KB + 1 KB alignment); at 64 and 32 two Q buffers and an
+//     8-slot ring (160 KB and 80 KB).
 //   * Warps (384 threads): 0-7 softmax (each row shared by two threads, one per half
 //     of the key columns, exchanging maxima and sums through shared memory), 8 MMA
 //     issuer, 9 TMA producer.  Every wait is bounded and sleeps.  Warps signal the
@@ -37,10 +38,12 @@ constexpr uint32_t kColS0_1 = 0, kColS1_1 = 128, kColO_1 = 256;
 
 template <int HD>
 struct Cfg1 {
-  static_assert(HD == 256 || HD == 128, "the one-tile layout serves head dims 128 and 256");
+  // each output row is written by two threads in 32-column chunks: head dim >= 32
+  static_assert(HD == 256 || HD == 128 || HD == 64 || HD == 32,
+                "the one-tile layout serves head dims 32 to 256");
   using C = Cfg<HD>;
   static constexpr int QBUF = HD == 256 ? 1 : 2;
-  static constexpr int NSLOT = HD == 256 ? 2 : 4;
+  static constexpr int NSLOT = HD == 256 ? 2 : HD == 128 ? 4 : 8;
   static constexpr int SMEM_BYTES = (QBUF + NSLOT) * C::TILE_BYTES + 1024;
 };
 
