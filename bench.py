@@ -260,6 +260,8 @@ def parse_args(argv=None):
                     "library's plan with splitting allowed, 1 = unsplit)")
     ap.add_argument("--kernel", choices=["auto", "two", "one"], default="auto",
                     help="sweep, unsplit: pin the two-tile or the one-tile kernel")
+    ap.add_argument("--order", choices=["auto", "one", "group"], default="auto",
+                    help="sweep, unsplit: pin the unit order (one snake / a snake per head group)")
     ap.add_argument("--sweep-shapes", default="", help="sweep: 'B,H,N;B,H,N;...' (overrides "
                     "--B, --H and --sweep-n)")
     ap.add_argument("--sweep-launches", type=int, default=20, help="timed launches per length "
@@ -537,7 +539,9 @@ def run_sweep(args):
                 kernel = fa.fwd_plan(B, H, N, d, causal)[0]
             elif splits > 1:
                 kernel = fa.FA_KERNEL_TWO_TILE
-        opts = fa.FwdOptions(kernel=kernel) if splits == 1 else None
+        order = {"auto": fa.FA_ORDER_AUTO, "one": fa.FA_ORDER_ONE_SNAKE,
+                 "group": fa.FA_ORDER_GROUP_SNAKES}[args.order]
+        opts = fa.FwdOptions(kernel=kernel, order=order) if splits == 1 else None
         if args.materialised:
             splits = 1
             ws = torch.empty(fa.materialised_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
@@ -551,7 +555,18 @@ def run_sweep(args):
         else:
             run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale,  # noqa: E731
                                     stream=stream, options=opts)
+        # the unit order the launch takes, where it is known here
+        shown = None
+        if args.materialised:
+            pass
+        elif order != fa.FA_ORDER_AUTO:
+            shown = order
+        elif args.kernel == "auto" and (splits == 1 or args.splits == 0):
+            shown = fa.fwd_plan(B, H, N, d, causal, allow_split=args.splits == 0,
+                                with_order=True)[2]
         rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal, "splits": splits,
+               "order": {fa.FA_ORDER_ONE_SNAKE: "one snake", fa.FA_ORDER_GROUP_SNAKES: "group snakes",
+                         None: None}[shown],
                "kernel": None if args.materialised else
                {fa.FA_KERNEL_TWO_TILE: "two-tile", fa.FA_KERNEL_ONE_TILE: "one-tile"}[kernel],
                "path": "materialised" if args.materialised else "tiled",

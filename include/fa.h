@@ -82,14 +82,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   kernel              FA_KERNEL_AUTO (0): the library's choice (fa_fwd_plan);
  *                       FA_KERNEL_TWO_TILE or FA_KERNEL_ONE_TILE pins that kernel
  *                       (FA_ERR_UNSUPPORTED for a head dim it does not serve).
- *   reserved            must be 0.
+ *   order               FA_ORDER_AUTO (0): the library's choice; FA_ORDER_ONE_SNAKE or
+ *                       FA_ORDER_GROUP_SNAKES pins how work units are handed to the
+ *                       CTAs (see fa_order).  Results are identical either way.
  */
 typedef struct {
     int64_t wait_budget_cycles;
     int32_t inject_skip_kv_load;
     int32_t max_ctas;
     int32_t kernel;
-    int32_t reserved;
+    int32_t order;
 } fa_fwd_options;
 
 /*
@@ -103,6 +105,20 @@ typedef enum {
                                 K/V tile); head dims 16-128; the only one with split-KV */
     FA_KERNEL_ONE_TILE = 2   /* 128 query rows per unit; head dims 32 to 256 */
 } fa_kernel;
+
+/*
+ * How a persistent launch hands its work units to the CTAs.  Units are numbered in
+ * groups of heads whose K and V fit in part of L2 together, longest unit first inside
+ * a group.  Round k gives each CTA one unit, in a snake (CTA c takes position c on even
+ * rounds, G-1-c on odd ones, G = CTAs).
+ */
+typedef enum {
+    FA_ORDER_AUTO = 0,
+    FA_ORDER_ONE_SNAKE = 1,     /* one snake over all units */
+    FA_ORDER_GROUP_SNAKES = 2   /* a snake restarted in each head group, CTA order mirrored
+                                   in odd groups: balances launches whose groups end in
+                                   part-filled rounds (e.g. one batch of 32 heads at 8192) */
+} fa_order;
 
 /* fa_fwd with options; opts may be NULL (same as fa_fwd). */
 int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -163,12 +179,17 @@ int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
  * and takes the shortest.  Few long units (one head at N = 8192) go to the one-tile
  * kernel, whose half-size units spread the causal triangle more evenly.
  *
- * Returns FA_OK, FA_ERR_INVALID_ARG (negative size, null output pointer) or
- * FA_ERR_UNSUPPORTED (head dim); an empty problem plans (FA_KERNEL_TWO_TILE, 1), or
- * (FA_KERNEL_ONE_TILE, 1) at head dim 256.
+ * *order (may be NULL) receives the unit order the launch takes (FA_ORDER_ONE_SNAKE or
+ * FA_ORDER_GROUP_SNAKES): the one whose modelled busiest CTA finishes first, on a grid of
+ * min(SMs, units) CTAs.
+ *
+ * Returns FA_OK, FA_ERR_INVALID_ARG (negative size, null kernel or splits pointer),
+ * FA_ERR_UNSUPPORTED (head dim, sizes) or, with num_sms = 0, the error of the device
+ * query; an empty problem plans (FA_KERNEL_TWO_TILE, 1), or (FA_KERNEL_ONE_TILE, 1) at
+ * head dim 256, with FA_ORDER_ONE_SNAKE.
  */
 int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allow_split,
-                int num_sms, int* kernel, int* splits);
+                int num_sms, int* kernel, int* splits, int* order);
 
 /*
  * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that may not allocate device

@@ -1,0 +1,91 @@
+"""GPU checks of the two unit orders (fa_fwd_options.order / fa_order).
+
+A launch hands its work units to the CTAs either in one snake over all units or in a
+snake per head group with odd groups mirrored; the library picks one per launch from a
+schedule model.  Which CTA computes a unit must not change a bit of the result, so
+each order is pinned here on shapes with several head groups -- including a ragged
+last group -- and compared with the other and with the fp64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _parity
+import oracle
+import tiled_online_softmax_fa_gb300 as fa
+import workloads
+
+pytestmark = pytest.mark.gpu
+W = workloads.WORKLOADS
+TWO, ONE = fa.FA_KERNEL_TWO_TILE, fa.FA_KERNEL_ONE_TILE
+SNAKE, GROUPS = fa.FA_ORDER_ONE_SNAKE, fa.FA_ORDER_GROUP_SNAKES
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.load_library()
+
+
+def _run(q, k, v, causal, **opt):
+    o, lse = fa.fa_fwd(q, k, v, causal=causal, options=fa.FwdOptions(**opt))
+    assert fa.get_device_status() == fa.FA_OK
+    return o, lse
+
+
+@pytest.mark.parametrize("kernel", [TWO, ONE], ids=["two-tile", "one-tile"])
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (1, 20, 8192, 128, True),    # head groups of 16 + 4 (K and V of 16 heads ~ 64 MB)
+    (2, 20, 8192, 64, False),    # groups of 32 + 8 at d = 64, full mask
+    (1, 40, 1536, 128, True),    # one group: both orders are the same snake
+])
+def test_orders_give_identical_bits_and_match_oracle(kernel, B, H, N, d, causal):
+    w = W["n32k"]
+    q, k, v = workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=B * H + N + d)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    a, la = _run(qd, kd, vd, causal, kernel=kernel, order=SNAKE)
+    b, lb = _run(qd, kd, vd, causal, kernel=kernel, order=GROUPS)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    rows = workloads.select_rows(w, B=B, H=H, N=N, seed=B * H + N)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, causal, scale)
+    _parity.compare(*_parity.gather_rows(b, lb, rows), o64, lse64)
+
+
+def test_split_launch_with_group_snakes():
+    """Two key-range pieces at B1 H20 N8192: 1280 items in head groups of 1024 + 256,
+    where the schedule model picks the per-group snake (modelled busiest CTA 330 vs 374
+    steps)."""
+    w = W["n32k"]
+    q, k, v = workloads.make_inputs(w, B=1, H=20, N=8192, d=128, seed=77)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    scale = float(np.float32(1.0 / np.sqrt(128)))
+    o, lse = fa.fa_fwd_splitkv(qd, kd, vd, causal=True, scale=scale, splits=2)
+    assert fa.get_device_status() == fa.FA_OK
+    rows = workloads.select_rows(w, B=1, H=20, N=8192, seed=78)
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, True, scale)
+    _parity.compare(*_parity.gather_rows(o, lse, rows), o64, lse64)
+
+
+def test_auto_order_is_the_planned_one_and_changes_nothing():
+    w = W["n4k"]
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w, B=1, H=32, N=8192, d=128, seed=3))
+    kernel, splits, order = fa.fwd_plan(1, 32, 8192, 128, True, with_order=True)
+    assert (kernel, splits) == (TWO, 1)
+    a, la = fa.fa_fwd(q, k, v, causal=True)
+    b, lb = _run(q, k, v, True, kernel=kernel, order=order)
+    c, lc = _run(q, k, v, True, kernel=kernel, order=SNAKE if order == GROUPS else GROUPS)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    assert torch.equal(a, c) and torch.equal(la, lc)
+
+
+def test_grid_cap_with_group_snakes():
+    """Seven CTAs over two ragged head groups: many rounds per group, both orders."""
+    w = W["n1k"]
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w, B=1, H=20, N=8192, d=128, seed=5))
+    a, la = _run(q, k, v, True, order=SNAKE, max_ctas=7)
+    b, lb = _run(q, k, v, True, order=GROUPS, max_ctas=7)
+    c, lc = _run(q, k, v, True, order=GROUPS)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    assert torch.equal(a, c) and torch.equal(la, lc)

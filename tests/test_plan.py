@@ -152,10 +152,13 @@ def test_plan_rejects_bad_sizes(args, want):
 def test_plan_rejects_null_outputs_and_negative_sms():
     lib = fa.load_library()
     k = ctypes.c_int()
-    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, SMS, None, ctypes.byref(k)) == fa.FA_ERR_INVALID_ARG
-    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, SMS, ctypes.byref(k), None) == fa.FA_ERR_INVALID_ARG
-    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, -1, ctypes.byref(k),
-                           ctypes.byref(ctypes.c_int())) == fa.FA_ERR_INVALID_ARG
+    s = ctypes.c_int()
+    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, SMS, None, ctypes.byref(k), None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, SMS, ctypes.byref(k), None, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, -1, ctypes.byref(k), ctypes.byref(s),
+                           None) == fa.FA_ERR_INVALID_ARG
+    # the order output is optional
+    assert lib.fa_fwd_plan(1, 1, 128, 128, 1, 0, SMS, ctypes.byref(k), ctypes.byref(s), None) == fa.FA_OK
 
 
 # --- the kernel pin in fa_fwd_options: checked before any CUDA call -------------------
@@ -166,16 +169,51 @@ def _call_opts(d, **opt):
 
 def test_options_struct_layout():
     assert ctypes.sizeof(fa.FwdOptions) == 24
-    assert fa.FwdOptions.kernel.offset == 16 and fa.FwdOptions.reserved.offset == 20
+    assert fa.FwdOptions.kernel.offset == 16 and fa.FwdOptions.order.offset == 20
 
 
 @pytest.mark.parametrize("d,opt,want", [
     (128, dict(kernel=3), fa.FA_ERR_INVALID_ARG),
     (128, dict(kernel=-1), fa.FA_ERR_INVALID_ARG),
-    (128, dict(reserved=1), fa.FA_ERR_INVALID_ARG),
+    (128, dict(order=3), fa.FA_ERR_INVALID_ARG),
+    (128, dict(order=-1), fa.FA_ERR_INVALID_ARG),
     (16, dict(kernel=ONE), fa.FA_ERR_UNSUPPORTED),
     (256, dict(kernel=TWO), fa.FA_ERR_UNSUPPORTED),
 ])
 def test_kernel_pin_rejected_before_cuda(d, opt, want):
     assert _call_opts(d, **opt) == want
     assert fa.last_error()
+
+
+# --- unit order: one snake vs a snake per head group ------------------------------------
+# (B, H, N) at d = 128 causal -> measured faster order of the two-tile kernel (profile
+# `unit_order_d128`; TFLOP/s one snake vs group snakes in the comment)
+MEASURED_ORDER = {
+    (1, 32, 8192): fa.FA_ORDER_GROUP_SNAKES,    # 1154 vs 1266
+    (4, 32, 8192): fa.FA_ORDER_GROUP_SNAKES,    # 1218 vs 1307
+    (1, 16, 16384): fa.FA_ORDER_GROUP_SNAKES,   # 1217 vs 1358
+    (8, 32, 4096): fa.FA_ORDER_GROUP_SNAKES,    # 1116 vs 1187
+    (1, 8, 32768): fa.FA_ORDER_GROUP_SNAKES,    # 1252 vs 1396
+    (8, 32, 8192): fa.FA_ORDER_ONE_SNAKE,       # 1319 vs 1291
+}
+
+
+@pytest.mark.parametrize("shape,want", sorted(MEASURED_ORDER.items()))
+def test_order_picks_the_measured_faster(shape, want):
+    B, H, N = shape
+    kernel, splits, order = fa.fwd_plan(B, H, N, 128, True, with_order=True, num_sms=SMS)
+    assert (kernel, splits) == (TWO, 1)
+    assert order == want
+
+
+def test_one_head_group_takes_the_one_snake():
+    # K and V of all heads fit the ~64 MB L2 share: one group, the orders coincide
+    for B, H, N, d in [(1, 4, 8192, 128), (1, 32, 1024, 128), (2, 16, 4096, 64), (1, 1, 65536, 128)]:
+        assert fa.fwd_plan(B, H, N, d, True, with_order=True, num_sms=SMS)[2] == fa.FA_ORDER_ONE_SNAKE
+
+
+def test_order_is_reported_for_every_plan():
+    for d in (16, 32, 64, 128, 256):
+        for B, H, N in [(1, 20, 8192), (8, 32, 2048), (1, 3, 100)]:
+            k, s, o = fa.fwd_plan(B, H, N, d, False, allow_split=True, with_order=True, num_sms=SMS)
+            assert o in (fa.FA_ORDER_ONE_SNAKE, fa.FA_ORDER_GROUP_SNAKES)

@@ -32,6 +32,9 @@ SUPPORTED_HEAD_DIMS = (16, 32, 64, 128, 256)
 FA_KERNEL_AUTO = 0
 FA_KERNEL_TWO_TILE = 1  # 256 query rows per work unit; head dims 16-128; split-KV
 FA_KERNEL_ONE_TILE = 2  # 128 query rows per work unit; head dims 32 to 256
+FA_ORDER_AUTO = 0
+FA_ORDER_ONE_SNAKE = 1     # one snake over all work units
+FA_ORDER_GROUP_SNAKES = 2  # a snake per head group, odd groups mirrored
 
 
 class FwdOptions(ctypes.Structure):
@@ -40,7 +43,7 @@ class FwdOptions(ctypes.Structure):
                 ("inject_skip_kv_load", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32),
                 ("kernel", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("order", ctypes.c_int32)]
 
 
 class FAError(RuntimeError):
@@ -85,7 +88,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.fa_splitkv_auto_splits.argtypes = [i64, i64, i64, ctypes.c_int]
         lib.fa_splitkv_auto_splits.restype = ctypes.c_int
         lib.fa_fwd_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_int)]
         lib.fa_fwd_plan.restype = ctypes.c_int
         lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                                ctypes.c_int, ctypes.c_float, ctypes.c_int, vp]
@@ -178,18 +182,21 @@ def splitkv_auto_splits(B: int, H: int, N: int, causal: bool = True) -> int:
 
 
 def fwd_plan(B: int, H: int, N: int, d: int, causal: bool = True, allow_split: bool = False,
-             num_sms: int = 0) -> tuple[int, int]:
-    """(kernel, splits) the library picks for these sizes (fa_fwd_plan).
+             num_sms: int = 0, with_order: bool = False):
+    """(kernel, splits) the library picks for these sizes (fa_fwd_plan), or
+    (kernel, splits, order) with ``with_order``.
 
     allow_split=False gives fa_fwd's choice, True that of fa_fwd_splitkv with splits=0.
     num_sms=0 asks the current device; a positive count plans without touching CUDA.
     """
-    kernel, splits = ctypes.c_int(), ctypes.c_int()
+    kernel, splits, order = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     rc = load_library().fa_fwd_plan(int(B), int(H), int(N), int(d), int(bool(causal)),
                                     int(bool(allow_split)), int(num_sms), ctypes.byref(kernel),
-                                    ctypes.byref(splits))
+                                    ctypes.byref(splits), ctypes.byref(order))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_plan")
+    if with_order:
+        return kernel.value, splits.value, order.value
     return kernel.value, splits.value
 
 

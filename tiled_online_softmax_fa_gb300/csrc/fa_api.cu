@@ -170,10 +170,9 @@ int64_t group_heads_for(int64_t BH, int64_t N, int64_t d) {
 // kernel's 128-row units are half as long, which matters when there are few units per
 // SM: under the causal mask unit lengths run from 1 to N/128 key tiles, and the longest
 // units set the finishing time.  The choice replays the static schedule both kernels
-// follow (unit_coords / unit_of: grouped longest-first order; in round k the CTA at grid
-// position c takes item k * grid + c, or k * grid + grid - 1 - c when k is odd) and
-// compares the busiest CTA's total.  Cost unit: one (128-row Q tile x 128-key tile) step
-// of the two-tile kernel.
+// follow (unit_coords / item_of: grouped longest-first order handed out in snakes, each
+// kernel at its better item order) and compares the busiest CTA's total.  Cost unit:
+// one (128-row Q tile x 128-key tile) step of the two-tile kernel.
 struct CostModel {
   double two_unit;      // fixed cost of an unsplit two-tile unit
   double one_unit;      // fixed cost of a one-tile unit, in one-tile steps
@@ -219,27 +218,33 @@ int64_t unit_block(int64_t u, int64_t BH, int64_t nqb, int64_t gh) {
   return nqb - 1 - (u - g * gh * nqb) / heads;
 }
 
-// The busiest CTA's total cost when `items` items (costs cost(i), in launch order) are
-// handed out in the kernels' snake order over `grid` CTAs.
+// The busiest CTA's total cost when `items` items (costs cost(i), numbered as item_of
+// numbers them) are handed out over `grid` CTAs in item order `order` (item_of inverted:
+// item i of a group sits at round i / grid, position i % grid; order 0 is one group).
 template <class Cost>
-double snake_makespan(int64_t items, int grid, Cost cost) {
+double schedule_makespan(int64_t items, int grid, int order, int64_t group_items, Cost cost) {
   double load[kModelMaxSms] = {};
-  for (int64_t i = 0; i < items; ++i) {
-    const int64_t k = i / grid;
-    const int r = static_cast<int>(i - k * grid);
-    load[(k & 1) ? grid - 1 - r : r] += cost(i);
+  const int64_t span = order == 0 ? items : group_items;
+  int64_t g = 0;
+  for (int64_t base = 0; base < items; base += span, ++g) {
+    const int64_t n = std::min(span, items - base);
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t k = i / grid;
+      const int r = static_cast<int>(i - k * grid);
+      const int c = (k & 1) ? grid - 1 - r : r;
+      load[(g & 1) ? grid - 1 - c : c] += cost(base + i);
+    }
   }
   return *std::max_element(load, load + grid);
 }
 
-double model_two_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int causal, int sms,
-                      int splits) {
+double model_two_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int causal, int grid,
+                      int splits, int order) {
   const int64_t nqb = (N + fa_sm103::kUnitRows - 1) / fa_sm103::kUnitRows;
   const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
   const int64_t gh = group_heads_for(BH, N, d);
   const int64_t items = nqb * BH * splits;
-  const int grid = static_cast<int>(std::min<int64_t>(sms, items));
-  double t = snake_makespan(items, grid, [&](int64_t w) {
+  double t = schedule_makespan(items, grid, order, gh * nqb * splits, [&](int64_t w) {
     const int64_t u = w / splits, sp = w - u * splits;
     const int64_t row0 = unit_block(u, BH, nqb, gh) * fa_sm103::kUnitRows;
     const int64_t n0 = tiles_from(row0, N, nkv, causal);
@@ -256,16 +261,56 @@ double model_two_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int
   return t;
 }
 
-double model_one_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int causal, int sms) {
+double model_one_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int causal, int grid,
+                      int order) {
   const int64_t nqb = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1;
   const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
   const int64_t gh = group_heads_for(BH, N, d);
-  const int64_t items = nqb * BH;
-  const int grid = static_cast<int>(std::min<int64_t>(sms, items));
-  return cm.one_step * snake_makespan(items, grid, [&](int64_t u) {
+  return cm.one_step * schedule_makespan(nqb * BH, grid, order, gh * nqb, [&](int64_t u) {
            const int64_t row0 = unit_block(u, BH, nqb, gh) * fa_sm103::one::kUnitRows1;
            return static_cast<double>(tiles_from(row0, N, nkv, causal)) + cm.one_unit;
          });
+}
+
+// The item order (Params::order) with the shorter modelled makespan for a launch of
+// `kernel` on `grid` CTAs.  The orders differ only with two or more head groups: one
+// snake over everything balances best when every group spans many rounds (b8 h32
+// S8192: 54 rounds); a snake per group wins when groups end in part-filled rounds (b1
+// h32 S8192, two groups of 3.4 rounds: 1154 -> 1266 TFLOP/s on GB300).  Decisions are
+// kept in a small cache, so repeated shapes replay the schedule once.
+constexpr int64_t kOrderMaxItems = int64_t{1} << 20;
+struct OrderEntry {
+  int64_t BH, N, d;
+  int causal, grid, splits, kernel, order;
+  bool valid;
+};
+std::mutex g_order_mu;
+OrderEntry g_order_cache[32];
+int g_order_next = 0;
+
+int schedule_order(int kernel, int64_t BH, int64_t N, int64_t d, int causal, int grid, int splits) {
+  const int64_t gh = group_heads_for(BH, N, d);
+  const int64_t rows = kernel == FA_KERNEL_ONE_TILE ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
+  const int64_t items = (N + rows - 1) / rows * BH * splits;
+  if (gh >= BH || grid > kModelMaxSms || items > kOrderMaxItems) return 0;
+  causal = causal ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lock(g_order_mu);
+    for (const OrderEntry& e : g_order_cache)
+      if (e.valid && e.BH == BH && e.N == N && e.d == d && e.causal == causal && e.grid == grid &&
+          e.splits == splits && e.kernel == kernel)
+        return e.order;
+  }
+  const CostModel& cm = cost_model(d) ? *cost_model(d) : kCostD128;
+  double t[2];
+  for (int o = 0; o < 2; ++o)
+    t[o] = kernel == FA_KERNEL_ONE_TILE ? model_one_tile(cm, BH, N, d, causal, grid, o)
+                                         : model_two_tile(cm, BH, N, d, causal, grid, splits, o);
+  const int order = t[1] < t[0] ? 1 : 0;
+  std::lock_guard<std::mutex> lock(g_order_mu);
+  g_order_cache[g_order_next] = {BH, N, d, causal, grid, splits, kernel, order, true};
+  g_order_next = (g_order_next + 1) % 32;
+  return order;
 }
 
 // The launch for a non-empty problem.  allow_split: the call has (or may size) a
@@ -278,8 +323,14 @@ Plan plan_for(int64_t BH, int64_t N, int64_t d, int causal, int sms, bool allow_
   if (!cm || sms > kModelMaxSms || units > kModelUnitsPerSm * sms ||
       units * splits > kModelMaxItems)
     return {FA_KERNEL_TWO_TILE, splits};
-  const double two = model_two_tile(*cm, BH, N, d, causal, sms, splits);
-  const double one = model_one_tile(*cm, BH, N, d, causal, sms);
+  // each kernel at the better of the two item orders (the launch picks it the same way)
+  const int64_t units1 = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1 * BH;
+  const int grid2 = static_cast<int>(std::min<int64_t>(sms, units * splits));
+  const int grid1 = static_cast<int>(std::min<int64_t>(sms, units1));
+  const double two = std::min(model_two_tile(*cm, BH, N, d, causal, grid2, splits, 0),
+                              model_two_tile(*cm, BH, N, d, causal, grid2, splits, 1));
+  const double one = std::min(model_one_tile(*cm, BH, N, d, causal, grid1, 0),
+                              model_one_tile(*cm, BH, N, d, causal, grid1, 1));
   return one < two ? Plan{FA_KERNEL_ONE_TILE, 1} : Plan{FA_KERNEL_TWO_TILE, splits};
 }
 
@@ -305,6 +356,28 @@ fa_sm103::Params base_params(void* o, float* lse, int64_t BH, int64_t N, int64_t
   p.budget = (opts && opts->wait_budget_cycles > 0) ? opts->wait_budget_cycles : kDefaultBudget;
   p.inject = opts ? opts->inject_skip_kv_load : 0;
   return p;
+}
+
+// The item order (Params::order) and the rounds every role iterates over, for `grid` CTAs.
+void set_schedule(fa_sm103::Params& p, int grid, int order) {
+  p.order = order;
+  p.group_items = p.group_heads * p.nqb * p.splits;
+  if (order == 0) {
+    p.rounds_per_group = 0;
+    p.num_rounds = (p.num_items + grid - 1) / grid;
+  } else {
+    const int groups = (p.BH + p.group_heads - 1) / p.group_heads;
+    p.rounds_per_group = (p.group_items + grid - 1) / grid;
+    p.num_rounds = groups * p.rounds_per_group;
+  }
+}
+
+// The item order of a launch: pinned by opts->order, else schedule_order's choice.
+int pick_order(const fa_fwd_options* opts, int kernel, int64_t BH, int64_t N, int64_t d, int causal,
+               int grid, int splits) {
+  if (opts && opts->order == FA_ORDER_ONE_SNAKE) return 0;
+  if (opts && opts->order == FA_ORDER_GROUP_SNAKES) return 1;
+  return schedule_order(kernel, BH, N, d, causal, grid, splits);
 }
 
 int grid_for(const DeviceState& dev, const fa_fwd_options* opts, int items) {
@@ -340,6 +413,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
                               static_cast<size_t>(p.num_items) * fa_sm103::kUnitRows * HD
                         : nullptr;
   const int grid = grid_for(dev, opts, p.num_items);
+  set_schedule(p, grid, pick_order(opts, FA_KERNEL_TWO_TILE, BH, N, HD, causal, grid, splits));
   constexpr int kThr = fa_sm103::rowk::kThreadsR;
   if (splits > 1)
     fa_sm103::rowk::fa_fwd_row_kernel<HD, true><<<grid, kThr, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
@@ -375,9 +449,10 @@ int launch_one(const void* q, const void* k, const void* v, void* o, float* lse,
     if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
     smem_set = true;
   }
-  const fa_sm103::Params p =
+  fa_sm103::Params p =
       base_params(o, lse, BH, N, HD, fa_sm103::one::kUnitRows1, causal, scale, opts);
   const int grid = grid_for(dev, opts, p.num_units);
+  set_schedule(p, grid, pick_order(opts, FA_KERNEL_ONE_TILE, BH, N, HD, causal, grid, 1));
   fa_sm103::one::fa_fwd_1tile_kernel<HD><<<grid, fa_sm103::one::kThreads1, SMEM, stream>>>(mq, mk, mv, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
@@ -459,7 +534,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (lse && overlaps(lse, lse_bytes, o, bytes)) return set_error(FA_ERR_INVALID_ARG, "lse overlaps o");
   if (opts && (opts->wait_budget_cycles < 0 || opts->inject_skip_kv_load < 0 || opts->max_ctas < 0))
     return set_error(FA_ERR_INVALID_ARG, "negative option");
-  if (opts && opts->reserved != 0) return set_error(FA_ERR_INVALID_ARG, "reserved option not 0");
+  if (opts && (opts->order < FA_ORDER_AUTO || opts->order > FA_ORDER_GROUP_SNAKES))
+    return set_error(FA_ERR_INVALID_ARG, "unknown item order");
   if (kernel < FA_KERNEL_AUTO || kernel > FA_KERNEL_ONE_TILE)
     return set_error(FA_ERR_INVALID_ARG, "unknown kernel");
   if (kernel == FA_KERNEL_TWO_TILE && d == 256)
@@ -545,7 +621,7 @@ int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal) {
 }
 
 int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allow_split,
-                int num_sms, int* kernel, int* splits) {
+                int num_sms, int* kernel, int* splits, int* order) {
   t_last_error.clear();
   if (!kernel || !splits) return set_error(FA_ERR_INVALID_ARG, "null output pointer");
   if (B < 0 || H < 0 || N < 0 || num_sms < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
@@ -553,6 +629,7 @@ int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allo
   if (B == 0 || H == 0 || N == 0) {
     *kernel = d == 256 ? FA_KERNEL_ONE_TILE : FA_KERNEL_TWO_TILE;
     *splits = 1;
+    if (order) *order = FA_ORDER_ONE_SNAKE;
     return FA_OK;
   }
   if (B > INT32_MAX / H || N > (int64_t{1} << 30))
@@ -567,6 +644,14 @@ int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allo
   const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, sms, allow_split != 0);
   *kernel = pl.kernel;
   *splits = pl.splits;
+  if (order) {
+    const int64_t rows = pl.kernel == FA_KERNEL_ONE_TILE ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
+    const int64_t items = (N + rows - 1) / rows * B * H * pl.splits;
+    const int grid = static_cast<int>(std::min<int64_t>(sms, items));
+    *order = schedule_order(pl.kernel, B * H, N, d, causal, grid, pl.splits) == 1
+                 ? FA_ORDER_GROUP_SNAKES
+                 : FA_ORDER_ONE_SNAKE;
+  }
   return FA_OK;
 }
 

@@ -188,9 +188,9 @@ __device__ void load_role1(const CUtensorMap* tmQ, const CUtensorMap* tmK, const
   prefetch_tmap(tmV);
   RingState1 rs;
   uint32_t units = 0;
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_units) continue;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
     int bh, row0;
     unit_coords1(u, p, bh, row0);
     const int n = tiles_for(row0, p);
@@ -230,9 +230,9 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
   uint32_t ring = 0, units = 0, oe_cnt = 0;
   uint32_t p_cnt0 = 0, p_cnt1 = 0;  // p_full completions seen, per S buffer
   const uint32_t ring_addr = smem_u32(sRing);
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_units) continue;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
     int bh, row0;
     unit_coords1(u, p, bh, row0);
     const int n = tiles_for(row0, p);
@@ -304,9 +304,9 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
   const uint64_t c2 = f32x2(c, c);
   uint32_t s_cnt0 = 0, s_cnt1 = 0;  // s_full completions seen, per S buffer
   uint32_t o_cnt = 0, x_cnt = 0, pv_cnt = 0;
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_units; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_units) continue;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
     int bh, row0;
     unit_coords1(u, p, bh, row0);
     const int n = tiles_for(row0, p);

@@ -79,6 +79,10 @@ struct Params {
   int splits;         // KV ranges per unit (1 = no split)
   int num_items;      // num_units * splits
   int group_heads;    // heads whose units are interleaved (K/V of a group fit in L2)
+  int order;          // item order over the grid: 0 one snake, 1 a snake per head group
+  int group_items;    // items of a full head group (group_heads * nqb * splits)
+  int rounds_per_group;  // order 1: ceil(group_items / gridDim.x)
+  int num_rounds;     // rounds every role iterates over
   float* ws_o;        // splits > 1: per item, normalised partial O [256 rows][HD] (fp32)
   float* ws_lse;      // splits > 1: per item, partial logsumexp [256 rows]
   int causal;
@@ -110,11 +114,26 @@ __device__ __forceinline__ void unit_coords(int u, const Params& p, int& bh, int
   row0 = qb * kUnitRows;
 }
 
-// The k-th unit of this CTA (snake order over the grid); may be >= num_units.
-__device__ __forceinline__ int unit_of(int k) {
-  const int pos = (k & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                          : static_cast<int>(blockIdx.x);
-  return k * static_cast<int>(gridDim.x) + pos;
+// The item this CTA takes in round k (0 <= k < num_rounds), or -1.  Items are numbered
+// in the grouped longest-first order of unit_coords (the pieces of a split unit next to
+// each other); G = gridDim.x.
+//   order 0: one snake over all items -- round k gives CTA c item k G + c (k even) or
+//            k G + G - 1 - c (k odd);
+//   order 1: that snake restarted in every head group, with the CTA order mirrored in
+//            odd groups, so the CTAs that took the light end of one group's last round
+//            take the heaviest items of the next.  Each group then balances by itself.
+__device__ __forceinline__ int item_of(int k, const Params& p) {
+  const int G = static_cast<int>(gridDim.x), c0 = static_cast<int>(blockIdx.x);
+  if (p.order == 0) {
+    const int i = k * G + ((k & 1) ? G - 1 - c0 : c0);
+    return i < p.num_items ? i : -1;
+  }
+  const int g = k / p.rounds_per_group, kg = k - g * p.rounds_per_group;
+  const int c = (g & 1) ? G - 1 - c0 : c0;
+  const int i = kg * G + ((kg & 1) ? G - 1 - c : c);
+  const int base = g * p.group_items;
+  const int n = p.num_items - base < p.group_items ? p.num_items - base : p.group_items;
+  return i < n ? base + i : -1;
 }
 
 // Number of K/V tiles a Q tile starting at `row_start` visits (0 if it holds no row < N).
@@ -184,9 +203,9 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
   uint32_t ring = 0;          // K/V ring entries issued so far
   uint32_t units = 0;         // units whose Q was issued
   uint32_t skipped = 0xFFFFFFFFu;
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_items) continue;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
     Item it;
     item_coords<SPLIT>(u, p, it);
     if (it.k1 <= it.k0) continue;  // an empty KV range (more splits than tiles)
@@ -262,9 +281,9 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
   const uint32_t q_addr[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE_BYTES)};
   const uint32_t col_s[2] = {kColS0, kColS1}, col_o[2] = {kColO0, kColO1};
   const uint32_t ring_addr = smem_u32(sRing);
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_items) continue;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
     Item it;
     item_coords<SPLIT>(u, p, it);
     if (it.k1 <= it.k0) continue;

@@ -123,9 +123,9 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
   const float c = p.scale_log2;
   const uint64_t c2 = f32x2(c, c);
   uint32_t s_cnt = 0, u_cnt = 0;
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_items) continue;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
     Item it;
     item_coords<SPLIT>(u, p, it);
     const int e_t = it.end(t);
@@ -215,9 +215,9 @@ __device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Pa
   const int lrow = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   uint32_t cnt[2] = {0, 0};  // units finished per Q tile
-  for (int k = 0; k * static_cast<int>(gridDim.x) < p.num_items; ++k) {
-    const int u = unit_of(k);
-    if (u >= p.num_items) continue;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
     Item it;
     item_coords<SPLIT>(u, p, it);
 #pragma unroll 1
