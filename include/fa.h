@@ -135,13 +135,16 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
  * The pages do not describe this; it follows from the definition above (the
  * logsumexp of a union of key ranges), and it is what the lse output enables.
  *
- *   splits     1..64, or 0 to let the library choose (fa_fwd_plan with allow_split);
- *              1 runs fa_fwd and needs no workspace.  Head dim 256 has no split
- *              variant: splits > 1 returns FA_ERR_UNSUPPORTED and 0 means 1.
+ *   splits     1..64, or 0 to let the library choose the launch (fa_fwd_plan with
+ *              allow_split) among the split counts whose partial results fit the
+ *              workspace given (none: unsplit); 1 runs fa_fwd and needs no workspace.
+ *              Head dim 256 has no split variant: splits > 1 returns
+ *              FA_ERR_UNSUPPORTED and 0 means 1.
  *   workspace  device memory, 16-byte aligned, caller-owned, at least
- *              fa_splitkv_workspace_bytes(B, H, N, d, splits) bytes (for splits = 0,
- *              the count from fa_fwd_plan or fa_splitkv_auto_splits, which is never
- *              smaller); must not overlap any tensor.
+ *              fa_splitkv_workspace_bytes(B, H, N, d, splits) bytes for splits > 1 (for
+ *              splits = 0, size it with the count fa_fwd_plan reports to get the plan's
+ *              own launch; a smaller workspace limits the choice); must not overlap any
+ *              tensor.
  *              Its contents on entry do not matter; they are scratch after the call.
  * Other arguments, ownership and errors as fa_fwd.
  */
@@ -154,11 +157,11 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits);
 
 /*
- * The split count the two-tile kernel takes for splits = 0 on the current device (1 on
- * error): more than one only when the longest query block's key range would be the
- * critical path (few, long blocks for the number of SMs, e.g. one head at N = 32768).
- * At head dim 128 fa_fwd_plan may still run such a call unsplit on the one-tile
- * kernel; a workspace sized for this count always suffices.
+ * The split heuristic's count for these sizes on the current device (1 on error): more
+ * than one only when the longest query block's key range would be the critical path
+ * (few, long blocks for the number of SMs, e.g. one head at N = 32768).  It is one of
+ * the candidates fa_fwd_plan models; the plan may take another count or kernel, so size
+ * a splits = 0 workspace with fa_fwd_plan.
  */
 int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
 
@@ -173,7 +176,8 @@ int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
  * Head dim 16 always takes the two-tile kernel and 256 the one-tile kernel.  At 32, 64
  * and 128, when there are at most four 256-row units per SM, the library models the run
  * time of each candidate -- the two-tile kernel unsplit, split as fa_splitkv_auto_splits
- * says, and the one-tile kernel -- by replaying the kernels' static schedule (unit
+ * says or (with no more units than SMs) 2, 3, 4, 5, 6 or 8 ways, and the one-tile
+ * kernel -- by replaying the kernels' static schedule (unit
  * lengths in key tiles, a one-tile step costing 1.14-1.18 two-tile steps, fixed costs
  * per unit, per split piece and for the merge, all fitted per head dim to GB300 timings)
  * and takes the shortest.  Few long units (one head at N = 8192) go to the one-tile

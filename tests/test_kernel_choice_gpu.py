@@ -140,3 +140,31 @@ def test_pinned_one_tile_small_head_dims_large_logits_and_many_units(d):
     _parity.check_case(W["n32k"], True, B=1, H=4, N=1000, d=d, seed=300 + d, kernel=ONE)
     rows = workloads.select_rows(W["b8n8k"], B=4, H=40, N=1536, seed=d)
     _parity.check_case(W["n1k"], True, B=4, H=40, N=1536, d=d, seed=d, rows=rows, kernel=ONE)
+
+
+def test_automatic_split_limited_by_the_workspace():
+    """splits = 0 plans among the split counts the workspace holds: the plan for one head
+    at N = 8192 takes several pieces; with room for two, or none, the call still runs
+    (fewer pieces, or unsplit) and matches the oracle."""
+    w = W["n32k"]
+    B, H, N, d = 1, 1, 8192, 128
+    q, k, v = workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=91)
+    rows = workloads.select_rows(w, B=B, H=H, N=N, seed=92)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, True, scale)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    kernel, splits = fa.fwd_plan(B, H, N, d, True, allow_split=True)
+    assert kernel == TWO and splits > 2
+    for room in (splits, 2, 0):
+        nbytes = fa.splitkv_workspace_bytes(B, H, N, d, room) if room > 1 else 0
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+        o = torch.empty_like(qd)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        rc = fa.fa_fwd_splitkv_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, True, scale, 0,
+                                   ws.data_ptr() if nbytes else 0, nbytes,
+                                   torch.cuda.current_stream().cuda_stream)
+        assert rc == fa.FA_OK, fa.last_error()
+        torch.cuda.synchronize()
+        assert fa.get_device_status() == fa.FA_OK
+        _parity.compare(*_parity.gather_rows(o, lse, rows), o64, lse64)

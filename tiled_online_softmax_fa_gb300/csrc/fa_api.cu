@@ -313,25 +313,53 @@ int schedule_order(int kernel, int64_t BH, int64_t N, int64_t d, int causal, int
   return order;
 }
 
-// The launch for a non-empty problem.  allow_split: the call has (or may size) a
-// workspace, so the two-tile kernel may split as choose_splits says.
-Plan plan_for(int64_t BH, int64_t N, int64_t d, int causal, int sms, bool allow_split) {
+// Split counts the planner also models when there are no more 256-row units than SMs
+// (one or two heads at N <= 16384 run fastest split 3 to 6 ways, which the heuristic
+// of choose_splits never proposes there).
+constexpr int kSplitCandidates[] = {2, 3, 4, 5, 6, 8};
+
+// The launch for a non-empty problem.  max_splits: the most key-range pieces the call
+// can hold partial results for (1 = no workspace).
+Plan plan_for(int64_t BH, int64_t N, int64_t d, int causal, int sms, int max_splits) {
   if (d == 256) return {FA_KERNEL_ONE_TILE, 1};
-  const int splits = allow_split ? choose_splits(BH, N, sms, causal) : 1;
+  int heur = max_splits > 1 ? choose_splits(BH, N, sms, causal) : 1;
+  if (heur > max_splits) heur = max_splits;
   const int64_t units = units_for(BH, N);
   const CostModel* cm = cost_model(d);
   if (!cm || sms > kModelMaxSms || units > kModelUnitsPerSm * sms ||
-      units * splits > kModelMaxItems)
-    return {FA_KERNEL_TWO_TILE, splits};
-  // each kernel at the better of the two item orders (the launch picks it the same way)
+      units * std::max(heur, 8) > kModelMaxItems)
+    return {FA_KERNEL_TWO_TILE, heur};
+  // each candidate at the better of the two item orders (the launch picks it the same way)
+  auto two_tile = [&](int splits) {
+    const int grid = static_cast<int>(std::min<int64_t>(sms, units * splits));
+    return std::min(model_two_tile(*cm, BH, N, d, causal, grid, splits, 0),
+                    model_two_tile(*cm, BH, N, d, causal, grid, splits, 1));
+  };
+  Plan best = {FA_KERNEL_TWO_TILE, 1};
+  double t_best = two_tile(1);
+  auto consider = [&](int splits) {
+    if (splits <= 1 || splits > max_splits) return;
+    const double t = two_tile(splits);
+    if (t < t_best) {
+      t_best = t;
+      best = {FA_KERNEL_TWO_TILE, splits};
+    }
+  };
+  consider(heur);
+  if (units <= sms)
+    for (const int sp : kSplitCandidates) consider(sp);
   const int64_t units1 = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1 * BH;
-  const int grid2 = static_cast<int>(std::min<int64_t>(sms, units * splits));
   const int grid1 = static_cast<int>(std::min<int64_t>(sms, units1));
-  const double two = std::min(model_two_tile(*cm, BH, N, d, causal, grid2, splits, 0),
-                              model_two_tile(*cm, BH, N, d, causal, grid2, splits, 1));
   const double one = std::min(model_one_tile(*cm, BH, N, d, causal, grid1, 0),
                               model_one_tile(*cm, BH, N, d, causal, grid1, 1));
-  return one < two ? Plan{FA_KERNEL_ONE_TILE, 1} : Plan{FA_KERNEL_TWO_TILE, splits};
+  return one < t_best ? Plan{FA_KERNEL_ONE_TILE, 1} : best;
+}
+
+// The most pieces whose partial results fit `bytes` of workspace (1 if none fit).
+int splits_fitting(int64_t BH, int64_t N, int64_t d, int64_t bytes) {
+  int s = kMaxSplits;
+  while (s > 1 && workspace_bytes(BH, N, d, s) > bytes) --s;
+  return s;
 }
 
 // Fields every launch shares.  `unit_rows` = query rows per work unit (256 for the
@@ -565,14 +593,17 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (st != FA_OK) return st;
   if (!dev->arch_ok) return set_error(FA_ERR_ARCH, "device is not sm_103 (GB300-class)");
   if (splits == 0) {
-    const Plan pl = plan_for(BH, N, d, causal, dev->num_sms, true);
+    // plan among the split counts the workspace can hold
+    const int max_splits =
+        workspace ? splits_fitting(BH, N, d, static_cast<int64_t>(workspace_size)) : 1;
+    const Plan pl = plan_for(BH, N, d, causal, dev->num_sms, max_splits);
     kernel = pl.kernel;
     splits = pl.splits;
     if (splits > 1 && !workspace_fits(workspace, workspace_size, BH, N, d, splits, q, k, v, o,
                                       bytes, lse, lse_bytes))
       return FA_ERR_INVALID_ARG;
   } else if (kernel == FA_KERNEL_AUTO) {
-    kernel = splits == 1 ? plan_for(BH, N, d, causal, dev->num_sms, false).kernel
+    kernel = splits == 1 ? plan_for(BH, N, d, causal, dev->num_sms, 1).kernel
                          : static_cast<int>(FA_KERNEL_TWO_TILE);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -641,7 +672,7 @@ int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allo
     if (st != FA_OK) return st;
     sms = dev->num_sms;
   }
-  const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, sms, allow_split != 0);
+  const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, sms, allow_split ? kMaxSplits : 1);
   *kernel = pl.kernel;
   *splits = pl.splits;
   if (order) {
@@ -715,7 +746,8 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   if (st != FA_OK) return st;
   int kernel = FA_KERNEL_AUTO;
   if (splits == 0) {
-    const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, dev->num_sms, true);
+    const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, dev->num_sms,
+                             splits_fitting(B * H, N, d, static_cast<int64_t>(kStaticScratchBytes)));
     kernel = pl.kernel;
     splits = pl.splits;
   }
