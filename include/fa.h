@@ -18,6 +18,13 @@
  * All functions are plain C and take raw pointers and sizes.  Compute is asynchronous
  * on the caller's stream.  None allocates device memory, except that the first call of
  * fa_fwd_materialised on a device creates a cuBLAS handle (see there).
+ *
+ * CUDA graphs: fa_fwd, fa_fwd_opts, fa_fwd_splitkv and fa_fwd_splitkv_noalloc may be
+ * captured into a graph on the caller's stream and replayed (the launch is planned at
+ * capture time from the sizes).  Make one call per device, head dim and entry point
+ * before the capture: the first call sets the kernels' shared-memory attribute and
+ * probes the device, which a capture should not see.  fa_get_device_status copies
+ * from the device and must not be called while capturing.
  */
 #ifndef FA_SM103_H
 #define FA_SM103_H
