@@ -39,8 +39,11 @@ def _run(q, k, v, causal, **opt):
     (1, 20, 8192, 128, True),    # head groups of 16 + 4 (K and V of 16 heads ~ 64 MB)
     (2, 20, 8192, 64, False),    # groups of 32 + 8 at d = 64, full mask
     (1, 40, 1536, 128, True),    # one group: both orders are the same snake
+    (1, 20, 4096, 256, True),    # d = 256: groups of 16 + 4 heads
 ])
 def test_orders_give_identical_bits_and_match_oracle(kernel, B, H, N, d, causal):
+    if d == 256 and kernel == TWO:
+        pytest.skip("head dim 256 runs the one-tile kernel only")
     w = W["n32k"]
     q, k, v = workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=B * H + N + d)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
