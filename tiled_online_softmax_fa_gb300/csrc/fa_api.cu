@@ -181,12 +181,14 @@ struct CostModel {
   double merge_fixed;   // the merge launch
   double merge_per_mb;  // per MB of fp32 partial outputs (written, merged)
 };
-// Fitted to GB300 timings: at d = 128, 82 two-vs-one pairs over 44 shapes (B 1-2, H 1-64,
-// N 256-65536, causal and not) and 18 split-vs-one-tile pairs; at d = 64 and 32, 88
-// two-vs-one pairs over the same shapes and 20 split-vs-one-tile pairs.  With them the
-// model picks the faster launch in every pair measured but one near-tie (0.4 %).
-constexpr CostModel kCostD128 = {1.0, 0.0, 1.18, 6.0, 5.0, 1.0};
-constexpr CostModel kCostD32To64 = {4.0, 1.0, 1.14, 12.0, 30.0, 0.5};
+// Fitted to GB300 timings.  Unit and step costs: at d = 128, 82 two-vs-one pairs over 44
+// shapes (B 1-2, H 1-64, N 256-65536, causal and not); at d = 64 and 32, 88 pairs over
+// the same shapes; the model picks the faster kernel in all but one near-tie (0.4 %).
+// Split costs: one or two to eight heads at N = 4096-32768 (16 shapes per head dim),
+// each timed unsplit, split 2, 3, 4, 5, 6 and 8 ways and on the one-tile kernel; the
+// model's pick is the measured best at d = 128 and within 0.2 % of it at d = 64 and 32.
+constexpr CostModel kCostD128 = {1.0, 0.0, 1.18, 6.0, 15.0, 0.25};
+constexpr CostModel kCostD32To64 = {4.0, 1.0, 1.14, 8.0, 10.0, 0.25};
 constexpr int kModelMaxSms = 1024;
 constexpr int64_t kModelUnitsPerSm = 4;      // more 256-row units per SM: two-tile kernel
 constexpr int64_t kModelMaxItems = 1 << 16;  // bound on the replayed schedule's length

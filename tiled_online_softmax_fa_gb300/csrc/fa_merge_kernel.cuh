@@ -15,10 +15,36 @@ namespace fa_sm103 {
 
 constexpr int kMergeThreads = 256;  // 8 rows per block
 
+// E consecutive fp32 values of a partial output (E = 1, 2 or 4 per lane).
+template <int E>
+__device__ __forceinline__ void load_partial(const float* src, float (&x)[E]) {
+  if constexpr (E == 4) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else if constexpr (E == 2) {
+    const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
+    x[0] = v.x; x[1] = v.y;
+  } else {
+    x[0] = __ldcs(src);
+  }
+}
+
+constexpr int kMergeEager = 8;  // up to this many pieces, partial outputs load up front
+
+// One warp per query row.  The row's pieces are found in the lanes (lane s holds piece s
+// and s + 32): their lse values give the row maximum and the weights exp(lse_s - m)
+// through two warp reductions.  Each lane reads its E columns of every piece and writes
+// its E bf16 outputs with one vector store.  With at most kMergeEager pieces the
+// partial outputs are loaded before the lse values are known, so a row costs one memory
+// round trip instead of two; a piece without an admissible key for the row (its key
+// range starts past the row's diagonal tile, its partial never written) has weight 0
+// and its loaded values are not used.
 template <int HD>
 __global__ void __launch_bounds__(kMergeThreads)
     fa_merge_kernel(const Params p) {
-  constexpr int E = HD >= 32 ? HD / 32 : 1;       // output elements per lane
+  static_assert(HD <= 128, "split launches serve head dims 16 to 128");
+  constexpr int E = HD >= 128 ? 4 : (HD >= 64 ? 2 : 1);  // output elements per lane
+  constexpr int kLanes = HD / E;                          // lanes that hold columns
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
   if (gw >= static_cast<int64_t>(p.BH) * p.N) return;
@@ -28,42 +54,78 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int g = bh / p.group_heads, first = g * p.group_heads;
   const int heads = (p.BH - first) < p.group_heads ? (p.BH - first) : p.group_heads;
   const int u = g * p.group_heads * p.nqb + (p.nqb - 1 - qb) * heads + (bh - first);
-  const bool active = lane * E < HD;
-
-  float m = -INFINITY;
-  for (int sp = 0; sp < p.splits; ++sp) {
-    Item it;
-    item_coords<true>(u * p.splits + sp, p, it);
-    if (it.end(t) <= it.k0) continue;  // no key of this range is admissible for the row
-    m = fmaxf(m, p.ws_lse[static_cast<size_t>(u * p.splits + sp) * kUnitRows + rin]);
+  const size_t base = static_cast<size_t>(u) * p.splits;
+  const bool active = lane < kLanes;
+  const bool eager = p.splits <= kMergeEager;
+  float xe[kMergeEager][E];
+  if (eager && active) {
+#pragma unroll
+    for (int sp = 0; sp < kMergeEager; ++sp)
+      if (sp < p.splits)
+        load_partial<E>(p.ws_o + ((base + sp) * kUnitRows + rin) * HD + lane * E, xe[sp]);
   }
+
+  // pieces s = lane and lane + 32: their lse, or -inf without an admissible key
+  float ls[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int sp = lane + 32 * h;
+    if (sp < p.splits) {
+      Item it;
+      item_coords<true>(static_cast<int>(base) + sp, p, it);
+      if (it.end(t) > it.k0) ls[h] = p.ws_lse[(base + sp) * kUnitRows + rin];
+    }
+  }
+  float m = fmaxf(ls[0], ls[1]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  float w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) w[h] = ls[h] == -INFINITY ? 0.f : expf(ls[h] - m);
+  float denom = w[0] + w[1];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xFFFFFFFFu, denom, off);
+
   float acc[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) acc[i] = 0.f;
-  float denom = 0.f;
-  for (int sp = 0; sp < p.splits; ++sp) {
-    Item it;
-    item_coords<true>(u * p.splits + sp, p, it);
-    if (it.end(t) <= it.k0) continue;
-    const size_t slot = static_cast<size_t>(u * p.splits + sp) * kUnitRows + rin;
-    const float wgt = expf(p.ws_lse[slot] - m);
-    denom += wgt;
-    if (active) {
-      const float* src = p.ws_o + slot * HD + lane * E;
-      if constexpr (E == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] += wgt * x.x; acc[1] += wgt * x.y; acc[2] += wgt * x.z; acc[3] += wgt * x.w;
-      } else {
+  if (eager) {
 #pragma unroll
-        for (int i = 0; i < E; ++i) acc[i] += wgt * src[i];
+    for (int sp = 0; sp < kMergeEager; ++sp) {
+      if (sp >= p.splits) break;
+      const float wgt = __shfl_sync(0xFFFFFFFFu, w[0], sp);
+      if (wgt != 0.f && active) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) acc[i] += wgt * xe[sp][i];
+      }
+    }
+  } else {
+#pragma unroll 4
+    for (int sp = 0; sp < p.splits; ++sp) {
+      const float wgt = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w[0] : w[1], sp & 31);
+      if (wgt != 0.f && active) {
+        float x[E];
+        load_partial<E>(p.ws_o + ((base + sp) * kUnitRows + rin) * HD + lane * E, x);
+#pragma unroll
+        for (int i = 0; i < E; ++i) acc[i] += wgt * x[i];
       }
     }
   }
   const float inv = 1.f / denom;
-  __nv_bfloat16* dst = p.o + (static_cast<size_t>(bh) * p.N + row) * HD + lane * E;
   if (active) {
-#pragma unroll
-    for (int i = 0; i < E; ++i) dst[i] = __float2bfloat16_rn(acc[i] * inv);
+    __nv_bfloat16* dst = p.o + (static_cast<size_t>(bh) * p.N + row) * HD + lane * E;
+    if constexpr (E == 4) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+      uint2 v;
+      v.x = *reinterpret_cast<const uint32_t*>(&lo);
+      v.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(dst) = v;
+    } else if constexpr (E == 2) {
+      *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    } else {
+      dst[0] = __float2bfloat16_rn(acc[0] * inv);
+    }
   }
   if (lane == 0 && p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.N + row] = m + logf(denom);
 }
