@@ -40,7 +40,7 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, non-finite or negative scale, aliasing */
-    FA_ERR_UNSUPPORTED = 2,    /* head dim not in {16, 32, 64, 128, 256}, a split of head dim 256, or a size beyond the kernel's range */
+    FA_ERR_UNSUPPORTED = 2,    /* head dim not in {16, 32, 64, 128, 256}, a kernel pinned for a head dim it does not serve, or a size beyond the kernel's range */
     FA_ERR_MISALIGNED = 3,     /* a tensor base address not 16-byte aligned (lse: 4-byte) */
     FA_ERR_ARCH = 4,           /* current device is not compute capability 10.3 (sm_103) */
     FA_ERR_CUDA = 5,           /* a CUDA runtime / driver call failed; see fa_last_error() */
@@ -109,7 +109,7 @@ typedef struct {
 typedef enum {
     FA_KERNEL_AUTO = 0,
     FA_KERNEL_TWO_TILE = 1,  /* 256 query rows per unit (two 128-row Q tiles sharing each
-                                K/V tile); head dims 16-128; the only one with split-KV */
+                                K/V tile); head dims 16-128 */
     FA_KERNEL_ONE_TILE = 2   /* 128 query rows per unit; head dims 32 to 256 */
 } fa_kernel;
 
@@ -135,7 +135,8 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
 /*
  * Split-KV forward (the same result as fa_fwd, more parallelism for small B*H*N).
  *
- * Each 256-row query block's key range is cut into `splits` pieces processed by
+ * Each work unit's key range (256 query rows on the two-tile kernel, 128 on the one-tile
+ * kernel) is cut into `splits` pieces processed by
  * different CTAs; every piece writes its normalised partial output O_s and the
  * logsumexp lse_s of its scores to `workspace`, and a second kernel merges them:
  *     lse = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s.
@@ -145,8 +146,8 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
  *   splits     1..64, or 0 to let the library choose the launch (fa_fwd_plan with
  *              allow_split) among the split counts whose partial results fit the
  *              workspace given (none: unsplit); 1 runs fa_fwd and needs no workspace.
- *              Head dim 256 has no split variant: splits > 1 returns
- *              FA_ERR_UNSUPPORTED and 0 means 1.
+ *              An explicit count > 1 runs the two-tile kernel (the one-tile kernel at
+ *              head dim 256); fa_fwd_splitkv_opts can pin either.
  *   workspace  device memory, 16-byte aligned, caller-owned, at least
  *              fa_splitkv_workspace_bytes(B, H, N, d, splits) bytes for splits > 1 (for
  *              splits = 0, size it with the count fa_fwd_plan reports to get the plan's
@@ -159,8 +160,18 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
                    int splits, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes fa_fwd_splitkv needs for these sizes and `splits` (>= 1); -1 on bad
-   arguments or an unsupported split (head dim 256 with splits > 1). */
+/*
+ * fa_fwd_splitkv with options (opts may be NULL): opts->kernel pins the kernel, which
+ * then needs an explicit splits >= 1 (FA_ERR_INVALID_ARG for splits = 0);
+ * opts->order pins the unit order; the other fields as fa_fwd_opts.
+ */
+int fa_fwd_splitkv_opts(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                        int splits, void* workspace, size_t workspace_bytes, void* stream,
+                        const fa_fwd_options* opts);
+
+/* Workspace bytes fa_fwd_splitkv needs for these sizes and `splits` (>= 1), for either
+   kernel (a one-tile item holds 128 rows, a two-tile one 256); -1 on bad arguments. */
 int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits);
 
 /*

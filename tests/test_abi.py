@@ -102,7 +102,8 @@ def test_splitkv_workspace_bytes():
     assert fa.splitkv_workspace_bytes(1, 32, 1024, 128, 0) == -1
     assert fa.splitkv_workspace_bytes(0, 32, 1024, 128, 4) == 0
     assert fa.splitkv_workspace_bytes(1, 32, 1024, 256, 1) == 0
-    assert fa.splitkv_workspace_bytes(1, 32, 1024, 256, 4) == -1
+    # head dim 256 splits on the one-tile kernel: 128-row items, the same total rows
+    assert fa.splitkv_workspace_bytes(1, 32, 1024, 256, 4) == units * 4 * 256 * (256 + 1) * 4
 
 
 def _split(**kw):
@@ -120,7 +121,6 @@ def _split(**kw):
     (dict(splits=-1), fa.FA_ERR_INVALID_ARG),
     (dict(ws_ptr=0x20000), fa.FA_ERR_INVALID_ARG),      # workspace overlaps k
     (dict(d=40), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),             # no split variant for head dim 256
 ])
 def test_splitkv_argument_errors(kw, want):
     assert _split(**kw) == want

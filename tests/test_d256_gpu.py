@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import _parity
+import oracle
 import tiled_online_softmax_fa_gb300 as fa
 import workloads
 
@@ -108,23 +109,24 @@ def test_guard_regions_and_determinism():
     assert torch.equal(o, o2) and torch.equal(lse, l2)
 
 
-def test_split_entry_points_run_unsplit():
-    """Head dim 256 has no split variant: splits = 0 runs one piece, splits > 1 is refused."""
-    q, k, v = (t.cuda() for t in workloads.make_inputs(W["n1k"], B=1, H=2, N=700, d=D, seed=36))
-    ref, lref = fa.fa_fwd(q, k, v, causal=True)
-    o, lse = fa.fa_fwd_splitkv(q, k, v, causal=True, splits=0)
-    assert torch.equal(o, ref) and torch.equal(lse, lref)
-    with pytest.raises(fa.FAError) as e:
-        fa.fa_fwd_splitkv(q, k, v, causal=True, splits=2,
-                          workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED
-    o3 = torch.empty_like(q)
-    l3 = torch.empty_like(lref)
-    rc = fa.fa_fwd_splitkv_noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o3.data_ptr(),
-                                       l3.data_ptr(), 1, 2, 700, D, True, float(np.float32(1 / 16)),
-                                       0)
-    assert rc == fa.FA_OK and fa.get_device_status() == fa.FA_OK
-    assert torch.equal(o3, ref) and torch.equal(l3, lref)
-    rc = fa.fa_fwd_splitkv_noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o3.data_ptr(),
-                                       l3.data_ptr(), 1, 2, 700, D, True, 0.0625, 3)
-    assert rc == fa.FA_ERR_UNSUPPORTED
+def test_split_entry_points():
+    """splits = 0 plans the launch; an explicit split runs the one-tile kernel in pieces;
+    the allocation-free entry point matches; all against the unsplit result's oracle."""
+    w = W["n1k"]
+    q, k, v = workloads.make_inputs(w, B=1, H=2, N=700, d=D, seed=36)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    scale = float(np.float32(1 / 16))
+    rows = workloads.select_rows(w, B=1, H=2, N=700, seed=37)
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, True, scale)
+    for splits in (0, 2):
+        o, lse = fa.fa_fwd_splitkv(qd, kd, vd, causal=True, scale=scale, splits=splits)
+        assert fa.get_device_status() == fa.FA_OK
+        _parity.compare(*_parity.gather_rows(o, lse, rows), o64, lse64)
+    o3 = torch.empty_like(qd)
+    l3 = torch.empty((1, 2, 700), dtype=torch.float32, device="cuda")
+    rc = fa.fa_fwd_splitkv_noalloc_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o3.data_ptr(),
+                                       l3.data_ptr(), 1, 2, 700, D, True, scale, 3)
+    assert rc == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    _parity.compare(*_parity.gather_rows(o3, l3, rows), o64, lse64)

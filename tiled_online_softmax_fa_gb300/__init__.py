@@ -83,6 +83,10 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int,
                                        ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
         lib.fa_fwd_splitkv.restype = ctypes.c_int
+        lib.fa_fwd_splitkv_opts.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int,
+                                            ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp,
+                                            ctypes.POINTER(FwdOptions)]
+        lib.fa_fwd_splitkv_opts.restype = ctypes.c_int
         lib.fa_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.c_int]
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_int64
         lib.fa_splitkv_auto_splits.argtypes = [i64, i64, i64, ctypes.c_int]
@@ -201,21 +205,25 @@ def fwd_plan(B: int, H: int, N: int, d: int, causal: bool = True, allow_split: b
 
 
 def fa_fwd_splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal, scale, splits,
-                       ws_ptr, ws_bytes, stream: int = 0) -> int:
-    """Call fa_fwd_splitkv with raw device addresses; returns the status code."""
+                       ws_ptr, ws_bytes, stream: int = 0, options: FwdOptions | None = None) -> int:
+    """Call fa_fwd_splitkv (fa_fwd_splitkv_opts with ``options``) with raw device
+    addresses; returns the status code."""
     lib = load_library()
-    return int(lib.fa_fwd_splitkv(q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None,
-                                  lse_ptr or None, int(B), int(H), int(N), int(d),
-                                  int(bool(causal)), float(scale), int(splits), ws_ptr or None,
-                                  int(ws_bytes), stream or None))
+    args = (q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None, lse_ptr or None, int(B),
+            int(H), int(N), int(d), int(bool(causal)), float(scale), int(splits), ws_ptr or None,
+            int(ws_bytes), stream or None)
+    if options is None:
+        return int(lib.fa_fwd_splitkv(*args))
+    return int(lib.fa_fwd_splitkv_opts(*args, ctypes.byref(options)))
 
 
 def fa_fwd_splitkv(q, k, v, o=None, lse=None, causal: bool = True, scale: float | None = None,
-                   splits: int = 0, workspace=None, stream=None):
+                   splits: int = 0, workspace=None, stream=None, options: FwdOptions | None = None):
     """fa_fwd with each query block's key range split across CTAs and merged by lse.
 
     splits = 0 lets the library choose.  ``workspace`` (a CUDA uint8 tensor) is
-    allocated here when not given.  Returns (o, lse).
+    allocated here when not given.  ``options`` may pin the kernel (with splits >= 1)
+    and the unit order.  Returns (o, lse).
     """
     import torch
     B, H, N, d = q.shape
@@ -239,7 +247,7 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, causal: bool = True, scale: float 
             raise TypeError(f"{name} must be a contiguous CUDA bf16 tensor shaped like q")
     rc = fa_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                             lse.data_ptr(), B, H, N, d, causal, scale, splits, ws_ptr, ws_bytes,
-                            _stream_handle(stream, q.device))
+                            _stream_handle(stream, q.device), options)
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_splitkv")
     return o, lse

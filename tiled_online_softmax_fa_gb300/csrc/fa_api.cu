@@ -454,19 +454,21 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (splits > 1) {
     const int64_t warps = BH * N;
     const int64_t blocks = (warps + fa_sm103::kMergeThreads / 32 - 1) / (fa_sm103::kMergeThreads / 32);
-    fa_sm103::fa_merge_kernel<HD><<<static_cast<unsigned>(blocks), fa_sm103::kMergeThreads, 0,
-                                    stream>>>(p);
+    fa_sm103::fa_merge_kernel<HD, fa_sm103::kUnitRows><<<static_cast<unsigned>(blocks),
+                                                         fa_sm103::kMergeThreads, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
   }
   return FA_OK;
 }
 
-// The one-Q-tile kernel (128-row units, no split-KV variant): head dims 256 and 128.
+// The one-Q-tile kernel (128-row units): head dims 32 to 256, split or not.  A split
+// launch writes per-piece partial results to the workspace (items x 128 rows: partial O
+// then partial lse) and the merge kernel combines them.
 template <int HD>
 int launch_one(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
                int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
-               bool& smem_set, const fa_fwd_options* opts) {
+               bool& smem_set, const fa_fwd_options* opts, int splits, void* workspace) {
   constexpr int SMEM = fa_sm103::one::Cfg1<HD>::SMEM_BYTES;
   CUtensorMap mq, mk, mv;
   int st;
@@ -474,18 +476,39 @@ int launch_one(const void* q, const void* k, const void* v, void* o, float* lse,
   if ((st = encode_map(&mk, k, BH, N, HD)) != FA_OK) return st;
   if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
   if (!smem_set) {
-    const cudaError_t e = cudaFuncSetAttribute(fa_sm103::one::fa_fwd_1tile_kernel<HD>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = cudaFuncSetAttribute(fa_sm103::one::fa_fwd_1tile_kernel<HD, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_sm103::one::fa_fwd_1tile_kernel<HD, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
     smem_set = true;
   }
   fa_sm103::Params p =
       base_params(o, lse, BH, N, HD, fa_sm103::one::kUnitRows1, causal, scale, opts);
-  const int grid = grid_for(dev, opts, p.num_units);
-  set_schedule(p, grid, pick_order(opts, FA_KERNEL_ONE_TILE, BH, N, HD, causal, grid, 1));
-  fa_sm103::one::fa_fwd_1tile_kernel<HD><<<grid, fa_sm103::one::kThreads1, SMEM, stream>>>(mq, mk, mv, p);
-  const cudaError_t e = cudaGetLastError();
+  p.splits = splits;
+  p.num_items = p.num_units * splits;
+  p.ws_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.ws_lse = splits > 1 ? static_cast<float*>(workspace) +
+                              static_cast<size_t>(p.num_items) * fa_sm103::one::kUnitRows1 * HD
+                        : nullptr;
+  const int grid = grid_for(dev, opts, p.num_items);
+  set_schedule(p, grid, pick_order(opts, FA_KERNEL_ONE_TILE, BH, N, HD, causal, grid, splits));
+  constexpr int kThr = fa_sm103::one::kThreads1;
+  if (splits > 1)
+    fa_sm103::one::fa_fwd_1tile_kernel<HD, true><<<grid, kThr, SMEM, stream>>>(mq, mk, mv, p);
+  else
+    fa_sm103::one::fa_fwd_1tile_kernel<HD, false><<<grid, kThr, SMEM, stream>>>(mq, mk, mv, p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
+  if (splits > 1) {
+    const int64_t warps = BH * N;
+    const int64_t blocks = (warps + fa_sm103::kMergeThreads / 32 - 1) / (fa_sm103::kMergeThreads / 32);
+    fa_sm103::fa_merge_kernel<HD, fa_sm103::one::kUnitRows1>
+        <<<static_cast<unsigned>(blocks), fa_sm103::kMergeThreads, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
+  }
   return FA_OK;
 }
 
@@ -525,9 +548,9 @@ int device_state(DeviceState** out) {
 namespace {
 
 // Shared body of every forward entry point.  splits = 0 lets plan_for choose the kernel
-// and the split count (a split needs the workspace); splits = 1 runs unsplit on the
-// kernel plan_for picks without splits, or on `kernel` when that is not FA_KERNEL_AUTO;
-// splits > 1 runs the two-tile kernel split that many ways.
+// and the split count (among the counts the workspace holds); splits >= 1 runs that many
+// pieces on `kernel`, or, when that is FA_KERNEL_AUTO, unsplit on the kernel plan_for
+// picks and split on the two-tile kernel (the one-tile kernel at head dim 256).
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
             int64_t H, int64_t N, int64_t d, int causal, float scale, void* stream,
             const fa_fwd_options* opts, int splits, void* workspace, size_t workspace_size,
@@ -572,14 +595,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
     return set_error(FA_ERR_UNSUPPORTED, "the two-tile kernel serves head dims 16 to 128");
   if (kernel == FA_KERNEL_ONE_TILE && d < 32)
     return set_error(FA_ERR_UNSUPPORTED, "the one-tile kernel serves head dims 32 to 256");
-  if (kernel != FA_KERNEL_AUTO && splits != 1)
-    return set_error(FA_ERR_INVALID_ARG, "a pinned kernel runs unsplit");
   if (splits < 0 || splits > kMaxSplits)
     return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
-  if (d == 256) {
-    if (splits > 1) return set_error(FA_ERR_UNSUPPORTED, "split-KV is not available for head dim 256");
-    splits = 1;  // the automatic choice for head dim 256 is always one piece
-  }
   if (splits > 1 || (splits == 0 && workspace)) {
     if (!workspace) return set_error(FA_ERR_INVALID_ARG, "a split launch needs a workspace");
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
@@ -605,17 +622,20 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
                                       bytes, lse, lse_bytes))
       return FA_ERR_INVALID_ARG;
   } else if (kernel == FA_KERNEL_AUTO) {
+    // unsplit: the planner's kernel; split as asked: the two-tile kernel (the one-tile
+    // kernel at head dim 256, which the two-tile kernel does not serve)
     kernel = splits == 1 ? plan_for(BH, N, d, causal, dev->num_sms, 1).kernel
+             : d == 256  ? static_cast<int>(FA_KERNEL_ONE_TILE)
                          : static_cast<int>(FA_KERNEL_TWO_TILE);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kernel == FA_KERNEL_ONE_TILE) {
     bool& set_one = dev->smem_set_one[hd];
     switch (hd) {
-      case 1: return launch_one<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
-      case 2: return launch_one<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
-      case 3: return launch_one<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
-      default: return launch_one<256>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts);
+      case 1: return launch_one<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts, splits, workspace);
+      case 2: return launch_one<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts, splits, workspace);
+      case 3: return launch_one<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts, splits, workspace);
+      default: return launch_one<256>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts, splits, workspace);
     }
   }
   bool& smem_set = dev->smem_set[hd];
@@ -641,7 +661,6 @@ int fa_fwd_opts(const void* q, const void* k, const void* v, void* o, float* lse
 int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int splits) {
   if (B < 0 || H < 0 || N < 0 || head_dim_index(d) < 0 || splits < 1 || splits > kMaxSplits)
     return -1;
-  if (d == 256 && splits > 1) return -1;  // no split-KV variant for head dim 256
   if (B == 0 || H == 0 || N == 0) return 0;
   return workspace_bytes(B * H, N, d, splits);
 }
@@ -695,6 +714,19 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                  workspace_bytes_given);
 }
 
+int fa_fwd_splitkv_opts(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                        int splits, void* workspace, size_t workspace_bytes_given, void* stream,
+                        const fa_fwd_options* opts) {
+  const int kernel = opts ? opts->kernel : FA_KERNEL_AUTO;
+  if (splits == 0 && kernel != FA_KERNEL_AUTO) {
+    t_last_error.clear();
+    return set_error(FA_ERR_INVALID_ARG, "a pinned kernel needs an explicit split count");
+  }
+  return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, opts, splits, workspace,
+                 workspace_bytes_given, kernel);
+}
+
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
            int64_t N, int64_t d, int causal, float scale, void* stream) {
   return fa_fwd_opts(q, k, v, o, lse, B, H, N, d, causal, scale, stream, nullptr);
@@ -738,8 +770,6 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
   if (head_dim_index(d) < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64, 128 or 256");
   if (splits < 0 || splits > kMaxSplits) return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
-  if (d == 256 && splits > 1)
-    return set_error(FA_ERR_UNSUPPORTED, "split-KV is not available for head dim 256");
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   if (B > INT32_MAX / H || N > (int64_t{1} << 30))
     return set_error(FA_ERR_UNSUPPORTED, "sizes beyond the kernel's range");
@@ -765,7 +795,7 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   void* scratch = nullptr;
   if (splits > 1 && (st = static_scratch_address(&scratch)) != FA_OK) return st;
   return forward(q, k, v, o, lse, B, H, N, d, causal, scale, stream, nullptr, splits, scratch,
-                 splits > 1 ? kStaticScratchBytes : 0, splits == 1 ? kernel : FA_KERNEL_AUTO);
+                 splits > 1 ? kStaticScratchBytes : 0, kernel);
 }
 
 int64_t fa_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kStaticScratchBytes); }

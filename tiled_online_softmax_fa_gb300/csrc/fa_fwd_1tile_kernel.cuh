@@ -76,6 +76,22 @@ __device__ __forceinline__ void unit_coords1(int u, const Params& p, int& bh, in
   row0 = qb * kUnitRows1;
 }
 
+// Item w -> (head, first query row, key tiles [k0, k1)).  Without SPLIT an item is a
+// whole unit; with SPLIT item w is piece w % splits of unit w / splits, the unit's key
+// tiles cut as evenly as integers allow.  An item with k1 <= k0 (more pieces than key
+// tiles) is empty and every role skips it.  Under the causal mask every key tile of a
+// unit holds admissible keys for all its rows, so a non-empty piece does too.
+template <bool SPLIT>
+__device__ __forceinline__ void item_coords1(int w, const Params& p, int& bh, int& row0, int& k0,
+                                             int& k1) {
+  const int u = SPLIT ? w / p.splits : w;
+  const int sp = SPLIT ? w - u * p.splits : 0;
+  unit_coords1(u, p, bh, row0);
+  const int n = tiles_for(row0, p);
+  k0 = SPLIT ? sp * n / p.splits : 0;
+  k1 = SPLIT ? (sp + 1) * n / p.splits : n;
+}
+
 // ------------------------------------------------------------------------------------
 // half-row softmax helpers: each query row is shared by two threads, one per 64-column
 // half of a 128-key score tile
@@ -149,8 +165,8 @@ __device__ __forceinline__ bool warp_wait1(uint64_t* bar, uint32_t parity, const
 }
 
 // ------------------------------------------------------------------------------------
-// TMA producer (one lane).  Ring order per unit of n tiles: K0, K1, then for
-// j = 0 .. n-1: V_j, K_{j+2} (the order the MMA issuer consumes).
+// TMA producer (one lane).  Ring order per item of key tiles [k0, k1): K_k0, K_k0+1,
+// then for j = k0 .. k1-1: V_j, K_{j+2} (the order the MMA issuer consumes).
 // ------------------------------------------------------------------------------------
 struct RingState1 {
   uint32_t ring = 0;
@@ -178,7 +194,7 @@ __device__ __forceinline__ bool emit_kv1(const CUtensorMap* tm, int tile, int bh
   return true;
 }
 
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ void load_role1(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                            uint8_t* sQ, uint8_t* sRing, Barriers1& b, const Params& p) {
   using C = Cfg<HD>;
@@ -191,22 +207,22 @@ __device__ void load_role1(const CUtensorMap* tmQ, const CUtensorMap* tmK, const
   for (int k = 0; k < p.num_rounds; ++k) {
     const int u = item_of(k, p);
     if (u < 0) continue;
-    int bh, row0;
-    unit_coords1(u, p, bh, row0);
-    const int n = tiles_for(row0, p);
+    int bh, row0, k0, k1;
+    item_coords1<SPLIT>(u, p, bh, row0, k0, k1);
+    if (k1 <= k0) continue;
     const uint32_t qb = units % QB;
-    // this Q buffer is free once the S MMAs of the unit that used it last are done
+    // this Q buffer is free once the S MMAs of the item that used it last are done
     if (units >= QB && !wait1(&b.q_empty[qb], ((units / QB) - 1) & 1, p, b)) goto fail;
     mbar_arrive_expect_tx(&b.q_full[qb], C::TILE_BYTES);
     for (int c = 0; c < C::NCH; ++c)
       tma_load_3d(sQ + qb * C::TILE_BYTES + c * C::CHUNK_BYTES, tmQ, &b.q_full[qb], c * C::W,
                   row0, bh);
     ++units;
-    if (!emit_kv1<HD>(tmK, 0, bh, u, sRing, b, p, rs)) goto fail;
-    if (n > 1 && !emit_kv1<HD>(tmK, 1, bh, u, sRing, b, p, rs)) goto fail;
-    for (int j = 0; j < n; ++j) {
+    if (!emit_kv1<HD>(tmK, k0, bh, u, sRing, b, p, rs)) goto fail;
+    if (k0 + 1 < k1 && !emit_kv1<HD>(tmK, k0 + 1, bh, u, sRing, b, p, rs)) goto fail;
+    for (int j = k0; j < k1; ++j) {
       if (!emit_kv1<HD>(tmV, j, bh, u, sRing, b, p, rs)) goto fail;
-      if (j + 2 < n && !emit_kv1<HD>(tmK, j + 2, bh, u, sRing, b, p, rs)) goto fail;
+      if (j + 2 < k1 && !emit_kv1<HD>(tmK, j + 2, bh, u, sRing, b, p, rs)) goto fail;
     }
   }
   goto drain;
@@ -222,7 +238,7 @@ drain:
 // ------------------------------------------------------------------------------------
 // MMA issuer (one lane)
 // ------------------------------------------------------------------------------------
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1& b,
                           const Params& p) {
   using C = Cfg<HD>;
@@ -233,9 +249,10 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
   for (int k = 0; k < p.num_rounds; ++k) {
     const int u = item_of(k, p);
     if (u < 0) continue;
-    int bh, row0;
-    unit_coords1(u, p, bh, row0);
-    const int n = tiles_for(row0, p);
+    int bh, row0, k0, k1;
+    item_coords1<SPLIT>(u, p, bh, row0, k0, k1);
+    if (k1 <= k0) continue;
+    const int n = k1 - k0;  // key tiles of this item; tile j of the loops is k0 + j
     const uint32_t qb = units % QB;
     const uint32_t q_addr = smem_u32(sQ + qb * C::TILE_BYTES);
     if (!wait1(&b.q_full[qb], (units / QB) & 1, p, b)) goto fail;
@@ -257,7 +274,7 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
       const uint32_t vs = ring % NS;
       if (!wait1(&b.slot_full[vs], (ring / NS) & 1, p, b)) goto fail;
       ++ring;
-      if (j == 0) {  // O must have been read out by the previous unit's epilogue
+      if (j == 0) {  // O must have been read out by the previous item's epilogue
         if (!wait1(&b.o_empty, (oe_cnt & 1) ^ 1, p, b)) goto fail;
         ++oe_cnt;
       }
@@ -292,7 +309,7 @@ drain:
 // ------------------------------------------------------------------------------------
 // softmax / epilogue (warps 0-7)
 // ------------------------------------------------------------------------------------
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Params& p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = (warp >> 2) & 1, wq = warp & 3;
@@ -307,9 +324,10 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
   for (int k = 0; k < p.num_rounds; ++k) {
     const int u = item_of(k, p);
     if (u < 0) continue;
-    int bh, row0;
-    unit_coords1(u, p, bh, row0);
-    const int n = tiles_for(row0, p);
+    int bh, row0, k0, k1;
+    item_coords1<SPLIT>(u, p, bh, row0, k0, k1);
+    if (k1 <= k0) continue;
+    const int n = k1 - k0;  // key tiles of this item; tile j of the loop is k0 + j
     const int row = row0 + lrow;
     const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
     float m_ref = -INFINITY;
@@ -324,7 +342,7 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
       uint32_t s[64];
       tmem_ld_x64(tmem + lane_base + colS + 64 * h, s);
       tmem_wait_ld(s);
-      const int kv0 = j * kBlockN + 64 * h;
+      const int kv0 = (k0 + j) * kBlockN + 64 * h;
       const int lim = last_key - kv0;
       const bool warp_mask = __any_sync(0xFFFFFFFFu, kv0 + 63 > last_key);
       const float pm = warp_mask ? row_max64<true>(s, lim) : row_max64<false>(s, lim);
@@ -386,7 +404,27 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
     if (!warp_wait1(&b.o_full, o_cnt & 1, p, b)) goto fail;
     ++o_cnt;
     tc_fence_after_sync();
-    {
+    if constexpr (SPLIT) {
+      // this piece's normalised partial output (fp32) and the lse of its scores
+      const float inv_l = 1.f / l_round;
+      const bool store = row < p.N;
+      const size_t slot = static_cast<size_t>(u) * kUnitRows1 + lrow;
+      float* orow = p.ws_o + slot * HD;
+#pragma unroll
+      for (int c0 = 32 * h; c0 < HD; c0 += 64) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + c0, o);
+        tmem_wait_ld(o);
+        if (store) {
+#pragma unroll
+          for (int v4 = 0; v4 < 32; v4 += 4)
+            *reinterpret_cast<float4*>(orow + c0 + v4) =
+                make_float4(__uint_as_float(o[v4]) * inv_l, __uint_as_float(o[v4 + 1]) * inv_l,
+                            __uint_as_float(o[v4 + 2]) * inv_l, __uint_as_float(o[v4 + 3]) * inv_l);
+        }
+      }
+      if (h == 0 && store) p.ws_lse[slot] = (m_ref + lg2_approx(l_exact)) * kLn2;
+    } else {
       const float inv_l = 1.f / l_round;
       const bool store = row < p.N;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + row) * HD;
@@ -420,7 +458,7 @@ fail:
 }
 
 // ------------------------------------------------------------------------------------
-template <int HD>
+template <int HD, bool SPLIT>
 __global__ void __launch_bounds__(kThreads1, 1)
     fa_fwd_1tile_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
@@ -464,12 +502,12 @@ __global__ void __launch_bounds__(kThreads1, 1)
   const uint32_t tmem = b.tmem_base;
 
   if (warp < kSoftmaxWarps1) {
-    softmax_role1<HD>(tmem, b, xchg, p);
+    softmax_role1<HD, SPLIT>(tmem, b, xchg, p);
   } else if (warp == kMmaWarp1) {
-    if (lane == 0) mma_role1<HD>(sQ, sRing, tmem, b, p);
+    if (lane == 0) mma_role1<HD, SPLIT>(sQ, sRing, tmem, b, p);
     __syncwarp();
   } else if (warp == kLoadWarp1) {
-    if (lane == 0) load_role1<HD>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
+    if (lane == 0) load_role1<HD, SPLIT>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
     __syncwarp();
   }
 

@@ -9,16 +9,22 @@
 
 #include <cuda_bf16.h>
 
+#include "fa_fwd_1tile_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa_sm103 {
 
 constexpr int kMergeThreads = 256;  // 8 rows per block
 
-// E consecutive fp32 values of a partial output (E = 1, 2 or 4 per lane).
+// E consecutive fp32 values of a partial output (E = 1, 2, 4 or 8 per lane).
 template <int E>
 __device__ __forceinline__ void load_partial(const float* src, float (&x)[E]) {
-  if constexpr (E == 4) {
+  if constexpr (E == 8) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(src));
+    const float4 c = __ldcs(reinterpret_cast<const float4*>(src + 4));
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+  } else if constexpr (E == 4) {
     const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
     x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
   } else if constexpr (E == 2) {
@@ -39,17 +45,20 @@ constexpr int kMergeEager = 8;  // up to this many pieces, partial outputs load 
 // round trip instead of two; a piece without an admissible key for the row (its key
 // range starts past the row's diagonal tile, its partial never written) has weight 0
 // and its loaded values are not used.
-template <int HD>
+// UNIT_ROWS: the query rows of the split kernel's work unit -- kUnitRows (two-tile
+// kernel: a piece may hold no admissible key for tile 0's rows) or kUnitRows1 (one-tile
+// kernel: every non-empty piece holds some).
+template <int HD, int UNIT_ROWS>
 __global__ void __launch_bounds__(kMergeThreads)
     fa_merge_kernel(const Params p) {
-  static_assert(HD <= 128, "split launches serve head dims 16 to 128");
-  constexpr int E = HD >= 128 ? 4 : (HD >= 64 ? 2 : 1);  // output elements per lane
+  static_assert(HD <= 256, "head dims 16 to 256");
+  constexpr int E = HD >= 256 ? 8 : (HD >= 128 ? 4 : (HD >= 64 ? 2 : 1));  // per lane
   constexpr int kLanes = HD / E;                          // lanes that hold columns
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
   if (gw >= static_cast<int64_t>(p.BH) * p.N) return;
   const int bh = static_cast<int>(gw / p.N), row = static_cast<int>(gw - static_cast<int64_t>(bh) * p.N);
-  const int qb = row / kUnitRows, rin = row - qb * kUnitRows, t = rin / kBlockM;
+  const int qb = row / UNIT_ROWS, rin = row - qb * UNIT_ROWS, t = rin / kBlockM;
   // unit of (bh, qb): the inverse of unit_coords
   const int g = bh / p.group_heads, first = g * p.group_heads;
   const int heads = (p.BH - first) < p.group_heads ? (p.BH - first) : p.group_heads;
@@ -62,7 +71,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
     for (int sp = 0; sp < kMergeEager; ++sp)
       if (sp < p.splits)
-        load_partial<E>(p.ws_o + ((base + sp) * kUnitRows + rin) * HD + lane * E, xe[sp]);
+        load_partial<E>(p.ws_o + ((base + sp) * UNIT_ROWS + rin) * HD + lane * E, xe[sp]);
   }
 
   // pieces s = lane and lane + 32: their lse, or -inf without an admissible key
@@ -71,9 +80,17 @@ __global__ void __launch_bounds__(kMergeThreads)
   for (int h = 0; h < 2; ++h) {
     const int sp = lane + 32 * h;
     if (sp < p.splits) {
-      Item it;
-      item_coords<true>(static_cast<int>(base) + sp, p, it);
-      if (it.end(t) > it.k0) ls[h] = p.ws_lse[(base + sp) * kUnitRows + rin];
+      bool holds;
+      if constexpr (UNIT_ROWS == kUnitRows) {
+        Item it;
+        item_coords<true>(static_cast<int>(base) + sp, p, it);
+        holds = it.end(t) > it.k0;
+      } else {
+        int ibh, irow0, k0, k1;
+        one::item_coords1<true>(static_cast<int>(base) + sp, p, ibh, irow0, k0, k1);
+        holds = k1 > k0;
+      }
+      if (holds) ls[h] = p.ws_lse[(base + sp) * UNIT_ROWS + rin];
     }
   }
   float m = fmaxf(ls[0], ls[1]);
@@ -105,7 +122,7 @@ __global__ void __launch_bounds__(kMergeThreads)
       const float wgt = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w[0] : w[1], sp & 31);
       if (wgt != 0.f && active) {
         float x[E];
-        load_partial<E>(p.ws_o + ((base + sp) * kUnitRows + rin) * HD + lane * E, x);
+        load_partial<E>(p.ws_o + ((base + sp) * UNIT_ROWS + rin) * HD + lane * E, x);
 #pragma unroll
         for (int i = 0; i < E; ++i) acc[i] += wgt * x[i];
       }
@@ -114,7 +131,14 @@ __global__ void __launch_bounds__(kMergeThreads)
   const float inv = 1.f / denom;
   if (active) {
     __nv_bfloat16* dst = p.o + (static_cast<size_t>(bh) * p.N + row) * HD + lane * E;
-    if constexpr (E == 4) {
+    if constexpr (E == 8) {
+      uint4 v;
+      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(dst) = v;
+    } else if constexpr (E == 4) {
       const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
       const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
       uint2 v;
