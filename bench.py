@@ -537,11 +537,12 @@ def run_sweep(args):
             splits = args.splits
             if splits == 1 and kernel == fa.FA_KERNEL_AUTO:
                 kernel = fa.fwd_plan(B, H, N, d, causal)[0]
-            elif splits > 1:
-                kernel = fa.FA_KERNEL_TWO_TILE
+            elif splits > 1 and kernel == fa.FA_KERNEL_AUTO:
+                kernel = fa.FA_KERNEL_ONE_TILE if d == 256 else fa.FA_KERNEL_TWO_TILE
         order = {"auto": fa.FA_ORDER_AUTO, "one": fa.FA_ORDER_ONE_SNAKE,
                  "group": fa.FA_ORDER_GROUP_SNAKES}[args.order]
-        opts = fa.FwdOptions(kernel=kernel, order=order) if splits == 1 else None
+        opts = fa.FwdOptions(kernel=kernel, order=order) if (splits == 1 or args.kernel != "auto") \
+            else None
         if args.materialised:
             splits = 1
             ws = torch.empty(fa.materialised_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
@@ -550,8 +551,12 @@ def run_sweep(args):
         elif splits > 1:
             ws = torch.empty(fa.splitkv_workspace_bytes(B, H, N, d, splits), dtype=torch.uint8,
                              device=dev)
+            # with --splits 0 the library plans the launch itself (kernel, pieces, order);
+            # the workspace is sized for the pieces its plan takes
+            n_arg = 0 if args.splits == 0 else splits
             run = lambda: fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, causal=causal, scale=scale,  # noqa: E731
-                                            splits=splits, workspace=ws, stream=stream)
+                                            splits=n_arg, workspace=ws, stream=stream,
+                                            options=opts)
         else:
             run = lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale,  # noqa: E731
                                     stream=stream, options=opts)

@@ -192,14 +192,17 @@ int fa_splitkv_auto_splits(int64_t B, int64_t H, int64_t N, int causal);
  * without touching CUDA.
  *
  * Head dim 16 always takes the two-tile kernel and 256 the one-tile kernel.  At 32, 64
- * and 128, when there are at most four 256-row units per SM, the library models the run
- * time of each candidate -- the two-tile kernel unsplit, split as fa_splitkv_auto_splits
- * says or (with no more units than SMs) 2, 3, 4, 5, 6 or 8 ways, and the one-tile
- * kernel -- by replaying the kernels' static schedule (unit
+ * and 128 (and at 256 for the one-tile kernel's splits), when there are at most four
+ * 256-row units per SM, the library models the run time of each candidate -- the
+ * two-tile kernel unsplit, split as fa_splitkv_auto_splits says or (with no more units
+ * than SMs) 2, 3, 4, 5, 6 or 8 ways, and the one-tile kernel unsplit or (with at most
+ * two 128-row units per SM) split 2-8 ways -- by replaying the kernels' static schedule (unit
  * lengths in key tiles, a one-tile step costing 1.14-1.18 two-tile steps, fixed costs
  * per unit, per split piece and for the merge, all fitted per head dim to GB300 timings)
  * and takes the shortest.  Few long units (one head at N = 8192) go to the one-tile
- * kernel, whose half-size units spread the causal triangle more evenly.
+ * kernel, whose half-size units spread the causal triangle more evenly, split when a
+ * workspace allows.  Decisions are cached per shape (the first call of a shape replays
+ * the schedules: up to ~0.4 ms of host time).
  *
  * *order (may be NULL) receives the unit order the launch takes (FA_ORDER_ONE_SNAKE or
  * FA_ORDER_GROUP_SNAKES): the one whose modelled busiest CTA finishes first, on a grid of

@@ -154,7 +154,7 @@ def test_automatic_split_limited_by_the_workspace():
     o64, lse64 = oracle.attn_rows(q, k, v, rows, True, scale)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     kernel, splits = fa.fwd_plan(B, H, N, d, True, allow_split=True)
-    assert kernel == TWO and splits > 2
+    assert splits > 2
     for room in (splits, 2, 0):
         nbytes = fa.splitkv_workspace_bytes(B, H, N, d, room) if room > 1 else 0
         ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")

@@ -180,21 +180,25 @@ struct CostModel {
   double split_piece;   // fixed cost of one split piece
   double merge_fixed;   // the merge launch
   double merge_per_mb;  // per MB of fp32 partial outputs (written, merged)
+  double one_piece;     // fixed cost of a one-tile split piece, in one-tile steps
 };
 // Fitted to GB300 timings.  Unit and step costs: at d = 128, 82 two-vs-one pairs over 44
 // shapes (B 1-2, H 1-64, N 256-65536, causal and not); at d = 64 and 32, 88 pairs over
 // the same shapes; the model picks the faster kernel in all but one near-tie (0.4 %).
-// Split costs: one or two to eight heads at N = 4096-32768 (16 shapes per head dim),
-// each timed unsplit, split 2, 3, 4, 5, 6 and 8 ways and on the one-tile kernel; the
-// model's pick is the measured best at d = 128 and within 0.2 % of it at d = 64 and 32.
-constexpr CostModel kCostD128 = {1.0, 0.0, 1.18, 6.0, 15.0, 0.25};
-constexpr CostModel kCostD32To64 = {4.0, 1.0, 1.14, 8.0, 10.0, 0.25};
+// Split costs: one to eight heads at N = 4096-32768 (16 shapes per head dim), each timed
+// on both kernels unsplit and split 2-8 ways; the model's pick is within 0.1 % of the
+// measured best at d = 32, 64 and 256 and within 8 % at d = 128 (one 406-vs-438 TFLOP/s
+// shape; 0 elsewhere).  At d = 256 only the one-tile kernel runs: its step is the unit.
+constexpr CostModel kCostD128 = {1.0, 0.0, 1.18, 6.0, 15.0, 0.25, 3.0};
+constexpr CostModel kCostD32To64 = {4.0, 1.0, 1.14, 8.0, 10.0, 0.25, 3.0};
+constexpr CostModel kCostD256 = {0.0, 0.0, 1.0, 0.0, 10.0, 0.25, 4.0};
 constexpr int kModelMaxSms = 1024;
 constexpr int64_t kModelUnitsPerSm = 4;      // more 256-row units per SM: two-tile kernel
 constexpr int64_t kModelMaxItems = 1 << 16;  // bound on the replayed schedule's length
 
 // The cost table of a head dim both kernels serve, else null.
 const CostModel* cost_model(int64_t d) {
+  if (d == 256) return &kCostD256;
   if (d == 128) return &kCostD128;
   if (d == 32 || d == 64) return &kCostD32To64;
   return nullptr;
@@ -264,14 +268,22 @@ double model_two_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int
 }
 
 double model_one_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int causal, int grid,
-                      int order) {
+                      int order, int splits = 1) {
   const int64_t nqb = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1;
   const int64_t nkv = (N + fa_sm103::kBlockN - 1) / fa_sm103::kBlockN;
   const int64_t gh = group_heads_for(BH, N, d);
-  return cm.one_step * schedule_makespan(nqb * BH, grid, order, gh * nqb, [&](int64_t u) {
-           const int64_t row0 = unit_block(u, BH, nqb, gh) * fa_sm103::one::kUnitRows1;
-           return static_cast<double>(tiles_from(row0, N, nkv, causal)) + cm.one_unit;
-         });
+  const int64_t items = nqb * BH * splits;
+  double t = cm.one_step * schedule_makespan(items, grid, order, gh * nqb * splits, [&](int64_t w) {
+    const int64_t u = w / splits, sp = w - u * splits;
+    const int64_t row0 = unit_block(u, BH, nqb, gh) * fa_sm103::one::kUnitRows1;
+    const int64_t n = tiles_from(row0, N, nkv, causal);
+    const int64_t k0 = sp * n / splits, k1 = (sp + 1) * n / splits;
+    if (k1 <= k0) return 0.0;
+    return static_cast<double>(k1 - k0) + (splits > 1 ? cm.one_piece : cm.one_unit);
+  });
+  if (splits > 1)
+    t += cm.merge_fixed + cm.merge_per_mb * static_cast<double>(splits * BH * N * d * 4) * 1e-6;
+  return t;
 }
 
 // The item order (Params::order) with the shorter modelled makespan for a launch of
@@ -306,7 +318,7 @@ int schedule_order(int kernel, int64_t BH, int64_t N, int64_t d, int causal, int
   const CostModel& cm = cost_model(d) ? *cost_model(d) : kCostD128;
   double t[2];
   for (int o = 0; o < 2; ++o)
-    t[o] = kernel == FA_KERNEL_ONE_TILE ? model_one_tile(cm, BH, N, d, causal, grid, o)
+    t[o] = kernel == FA_KERNEL_ONE_TILE ? model_one_tile(cm, BH, N, d, causal, grid, o, splits)
                                          : model_two_tile(cm, BH, N, d, causal, grid, splits, o);
   const int order = t[1] < t[0] ? 1 : 0;
   std::lock_guard<std::mutex> lock(g_order_mu);
@@ -315,46 +327,84 @@ int schedule_order(int kernel, int64_t BH, int64_t N, int64_t d, int causal, int
   return order;
 }
 
-// Split counts the planner also models when there are no more 256-row units than SMs
-// (one or two heads at N <= 16384 run fastest split 3 to 6 ways, which the heuristic
-// of choose_splits never proposes there).
+// Split counts the planner also models when there are few units per SM (one or two
+// heads at N <= 16384 run fastest split 3 to 6 ways, which the heuristic of choose_splits
+// never proposes there).
 constexpr int kSplitCandidates[] = {2, 3, 4, 5, 6, 8};
 
 // The launch for a non-empty problem.  max_splits: the most key-range pieces the call
-// can hold partial results for (1 = no workspace).
+// can hold partial results for (1 = no workspace).  Candidates: the two-tile kernel
+// unsplit, split as choose_splits says and (with no more 256-row units than SMs) split
+// 2-8 ways; the one-tile kernel unsplit and (with at most two 128-row units per SM)
+// split 2-8 ways.  Each is modelled at its better item order; the shortest wins.
 Plan plan_for(int64_t BH, int64_t N, int64_t d, int causal, int sms, int max_splits) {
-  if (d == 256) return {FA_KERNEL_ONE_TILE, 1};
-  int heur = max_splits > 1 ? choose_splits(BH, N, sms, causal) : 1;
+  const bool two_ok = d <= 128, one_ok = d >= 32;
+  int heur = (max_splits > 1 && two_ok) ? choose_splits(BH, N, sms, causal) : 1;
   if (heur > max_splits) heur = max_splits;
   const int64_t units = units_for(BH, N);
+  const int64_t units1 = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1 * BH;
   const CostModel* cm = cost_model(d);
   if (!cm || sms > kModelMaxSms || units > kModelUnitsPerSm * sms ||
-      units * std::max(heur, 8) > kModelMaxItems)
-    return {FA_KERNEL_TWO_TILE, heur};
-  // each candidate at the better of the two item orders (the launch picks it the same way)
-  auto two_tile = [&](int splits) {
-    const int grid = static_cast<int>(std::min<int64_t>(sms, units * splits));
-    return std::min(model_two_tile(*cm, BH, N, d, causal, grid, splits, 0),
-                    model_two_tile(*cm, BH, N, d, causal, grid, splits, 1));
-  };
-  Plan best = {FA_KERNEL_TWO_TILE, 1};
-  double t_best = two_tile(1);
-  auto consider = [&](int splits) {
-    if (splits <= 1 || splits > max_splits) return;
-    const double t = two_tile(splits);
-    if (t < t_best) {
+      units1 * std::max(heur, 8) > kModelMaxItems)
+    return two_ok ? Plan{FA_KERNEL_TWO_TILE, heur} : Plan{FA_KERNEL_ONE_TILE, 1};
+  Plan best = {0, 0};
+  double t_best = 0.0;
+  auto consider = [&](int kernel, int splits) {
+    if (splits < 1 || splits > max_splits) return;
+    const int64_t items = (kernel == FA_KERNEL_ONE_TILE ? units1 : units) * splits;
+    const int grid = static_cast<int>(std::min<int64_t>(sms, items));
+    double t = 0.0;
+    for (int o = 0; o < 2; ++o) {
+      const double to = kernel == FA_KERNEL_ONE_TILE
+                            ? model_one_tile(*cm, BH, N, d, causal, grid, o, splits)
+                            : model_two_tile(*cm, BH, N, d, causal, grid, splits, o);
+      t = o == 0 ? to : std::min(t, to);
+    }
+    if (best.kernel == 0 || t < t_best) {
       t_best = t;
-      best = {FA_KERNEL_TWO_TILE, splits};
+      best = {kernel, splits};
     }
   };
-  consider(heur);
-  if (units <= sms)
-    for (const int sp : kSplitCandidates) consider(sp);
-  const int64_t units1 = (N + fa_sm103::one::kUnitRows1 - 1) / fa_sm103::one::kUnitRows1 * BH;
-  const int grid1 = static_cast<int>(std::min<int64_t>(sms, units1));
-  const double one = std::min(model_one_tile(*cm, BH, N, d, causal, grid1, 0),
-                              model_one_tile(*cm, BH, N, d, causal, grid1, 1));
-  return one < t_best ? Plan{FA_KERNEL_ONE_TILE, 1} : best;
+  if (two_ok) {
+    consider(FA_KERNEL_TWO_TILE, 1);
+    if (heur > 1) consider(FA_KERNEL_TWO_TILE, heur);
+    if (units <= sms)
+      for (const int sp : kSplitCandidates) consider(FA_KERNEL_TWO_TILE, sp);
+  }
+  if (one_ok) {
+    consider(FA_KERNEL_ONE_TILE, 1);
+    if (units1 <= 2 * sms)
+      for (const int sp : kSplitCandidates) consider(FA_KERNEL_ONE_TILE, sp);
+  }
+  return best;
+}
+
+// plan_for's decisions, kept per shape: replaying the schedules of all candidates costs
+// up to a millisecond of host time, which a loop of short launches must not pay per call.
+struct PlanEntry {
+  int64_t BH, N, d;
+  int causal, sms, max_splits;
+  Plan plan;
+  bool valid;
+};
+std::mutex g_plan_mu;
+PlanEntry g_plan_cache[64];
+int g_plan_next = 0;
+
+Plan plan_cached(int64_t BH, int64_t N, int64_t d, int causal, int sms, int max_splits) {
+  causal = causal ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (const PlanEntry& e : g_plan_cache)
+      if (e.valid && e.BH == BH && e.N == N && e.d == d && e.causal == causal && e.sms == sms &&
+          e.max_splits == max_splits)
+        return e.plan;
+  }
+  const Plan pl = plan_for(BH, N, d, causal, sms, max_splits);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plan_cache[g_plan_next] = {BH, N, d, causal, sms, max_splits, pl, true};
+  g_plan_next = (g_plan_next + 1) % 64;
+  return pl;
 }
 
 // The most pieces whose partial results fit `bytes` of workspace (1 if none fit).
@@ -615,7 +665,7 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
     // plan among the split counts the workspace can hold
     const int max_splits =
         workspace ? splits_fitting(BH, N, d, static_cast<int64_t>(workspace_size)) : 1;
-    const Plan pl = plan_for(BH, N, d, causal, dev->num_sms, max_splits);
+    const Plan pl = plan_cached(BH, N, d, causal, dev->num_sms, max_splits);
     kernel = pl.kernel;
     splits = pl.splits;
     if (splits > 1 && !workspace_fits(workspace, workspace_size, BH, N, d, splits, q, k, v, o,
@@ -624,7 +674,7 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   } else if (kernel == FA_KERNEL_AUTO) {
     // unsplit: the planner's kernel; split as asked: the two-tile kernel (the one-tile
     // kernel at head dim 256, which the two-tile kernel does not serve)
-    kernel = splits == 1 ? plan_for(BH, N, d, causal, dev->num_sms, 1).kernel
+    kernel = splits == 1 ? plan_cached(BH, N, d, causal, dev->num_sms, 1).kernel
              : d == 256  ? static_cast<int>(FA_KERNEL_ONE_TILE)
                          : static_cast<int>(FA_KERNEL_TWO_TILE);
   }
@@ -693,7 +743,7 @@ int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allo
     if (st != FA_OK) return st;
     sms = dev->num_sms;
   }
-  const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, sms, allow_split ? kMaxSplits : 1);
+  const Plan pl = plan_cached(B * H, N, d, causal ? 1 : 0, sms, allow_split ? kMaxSplits : 1);
   *kernel = pl.kernel;
   *splits = pl.splits;
   if (order) {
@@ -778,8 +828,8 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   if (st != FA_OK) return st;
   int kernel = FA_KERNEL_AUTO;
   if (splits == 0) {
-    const Plan pl = plan_for(B * H, N, d, causal ? 1 : 0, dev->num_sms,
-                             splits_fitting(B * H, N, d, static_cast<int64_t>(kStaticScratchBytes)));
+    const Plan pl = plan_cached(B * H, N, d, causal ? 1 : 0, dev->num_sms,
+                                splits_fitting(B * H, N, d, static_cast<int64_t>(kStaticScratchBytes)));
     kernel = pl.kernel;
     splits = pl.splits;
   }
