@@ -260,8 +260,9 @@ def parse_args(argv=None):
                     "library's plan with splitting allowed, 1 = unsplit)")
     ap.add_argument("--kernel", choices=["auto", "two", "one"], default="auto",
                     help="sweep, unsplit: pin the two-tile or the one-tile kernel")
-    ap.add_argument("--order", choices=["auto", "one", "group"], default="auto",
-                    help="sweep, unsplit: pin the unit order (one snake / a snake per head group)")
+    ap.add_argument("--order", choices=["auto", "one", "group", "shifted"], default="auto",
+                    help="sweep: pin the unit order (one snake / a snake per head group, odd "
+                    "groups mirrored / shifted past the previous group's last round)")
     ap.add_argument("--sweep-shapes", default="", help="sweep: 'B,H,N;B,H,N;...' (overrides "
                     "--B, --H and --sweep-n)")
     ap.add_argument("--sweep-launches", type=int, default=20, help="timed launches per length "
@@ -540,7 +541,7 @@ def run_sweep(args):
             elif splits > 1 and kernel == fa.FA_KERNEL_AUTO:
                 kernel = fa.FA_KERNEL_ONE_TILE if d == 256 else fa.FA_KERNEL_TWO_TILE
         order = {"auto": fa.FA_ORDER_AUTO, "one": fa.FA_ORDER_ONE_SNAKE,
-                 "group": fa.FA_ORDER_GROUP_SNAKES}[args.order]
+                 "group": fa.FA_ORDER_GROUP_SNAKES, "shifted": fa.FA_ORDER_SHIFTED_SNAKES}[args.order]
         opts = fa.FwdOptions(kernel=kernel, order=order) if (splits == 1 or args.kernel != "auto") \
             else None
         if args.materialised:
@@ -571,7 +572,7 @@ def run_sweep(args):
                                 with_order=True)[2]
         rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal, "splits": splits,
                "order": {fa.FA_ORDER_ONE_SNAKE: "one snake", fa.FA_ORDER_GROUP_SNAKES: "group snakes",
-                         None: None}[shown],
+                         fa.FA_ORDER_SHIFTED_SNAKES: "shifted snakes", None: None}[shown],
                "kernel": None if args.materialised else
                {fa.FA_KERNEL_TWO_TILE: "two-tile", fa.FA_KERNEL_ONE_TILE: "one-tile"}[kernel],
                "path": "materialised" if args.materialised else "tiled",

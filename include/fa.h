@@ -122,9 +122,12 @@ typedef enum {
 typedef enum {
     FA_ORDER_AUTO = 0,
     FA_ORDER_ONE_SNAKE = 1,     /* one snake over all units */
-    FA_ORDER_GROUP_SNAKES = 2   /* a snake restarted in each head group, CTA order mirrored
+    FA_ORDER_GROUP_SNAKES = 2,  /* a snake restarted in each head group, CTA order mirrored
                                    in odd groups: balances launches whose groups end in
                                    part-filled rounds (e.g. one batch of 32 heads at 8192) */
+    FA_ORDER_SHIFTED_SNAKES = 3 /* a snake restarted in each head group, each group starting
+                                   at the CTAs its predecessor's part-filled last round
+                                   left out: balances launches of many groups */
 } fa_order;
 
 /* fa_fwd with options; opts may be NULL (same as fa_fwd). */

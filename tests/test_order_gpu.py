@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
 W = workloads.WORKLOADS
 TWO, ONE = fa.FA_KERNEL_TWO_TILE, fa.FA_KERNEL_ONE_TILE
 SNAKE, GROUPS = fa.FA_ORDER_ONE_SNAKE, fa.FA_ORDER_GROUP_SNAKES
+SHIFTED = fa.FA_ORDER_SHIFTED_SNAKES
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -52,7 +53,9 @@ def test_orders_give_identical_bits_and_match_oracle(kernel, B, H, N, d, causal)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     a, la = _run(qd, kd, vd, causal, kernel=kernel, order=SNAKE)
     b, lb = _run(qd, kd, vd, causal, kernel=kernel, order=GROUPS)
+    c, lc = _run(qd, kd, vd, causal, kernel=kernel, order=SHIFTED)
     assert torch.equal(a, b) and torch.equal(la, lb)
+    assert torch.equal(a, c) and torch.equal(la, lc)
     rows = workloads.select_rows(w, B=B, H=H, N=N, seed=B * H + N)
     scale = float(np.float32(1.0 / np.sqrt(d)))
     o64, lse64 = oracle.attn_rows(q, k, v, rows, causal, scale)
@@ -81,9 +84,11 @@ def test_auto_order_is_the_planned_one_and_changes_nothing():
     assert (kernel, splits) == (TWO, 1)
     a, la = fa.fa_fwd(q, k, v, causal=True)
     b, lb = _run(q, k, v, True, kernel=kernel, order=order)
-    c, lc = _run(q, k, v, True, kernel=kernel, order=SNAKE if order == GROUPS else GROUPS)
+    others = [o for o in (SNAKE, GROUPS, SHIFTED) if o != order]
     assert torch.equal(a, b) and torch.equal(la, lb)
-    assert torch.equal(a, c) and torch.equal(la, lc)
+    for o in others:
+        c, lc = _run(q, k, v, True, kernel=kernel, order=o)
+        assert torch.equal(a, c) and torch.equal(la, lc)
 
 
 def test_grid_cap_with_group_snakes():
@@ -93,5 +98,7 @@ def test_grid_cap_with_group_snakes():
     a, la = _run(q, k, v, True, order=SNAKE, max_ctas=7)
     b, lb = _run(q, k, v, True, order=GROUPS, max_ctas=7)
     c, lc = _run(q, k, v, True, order=GROUPS)
+    e, le = _run(q, k, v, True, order=SHIFTED, max_ctas=7)
     assert torch.equal(a, b) and torch.equal(la, lb)
     assert torch.equal(a, c) and torch.equal(la, lc)
+    assert torch.equal(a, e) and torch.equal(la, le)

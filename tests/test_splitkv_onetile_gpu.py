@@ -79,8 +79,10 @@ def test_orders_and_grid_cap_give_the_same_bits():
     a, la = _split_one(q, k, v, True, scale, 3, order=fa.FA_ORDER_ONE_SNAKE)
     b, lb = _split_one(q, k, v, True, scale, 3, order=fa.FA_ORDER_GROUP_SNAKES)
     c, lc = _split_one(q, k, v, True, scale, 3, max_ctas=9)
+    e, le = _split_one(q, k, v, True, scale, 3, order=fa.FA_ORDER_SHIFTED_SNAKES, max_ctas=9)
     assert torch.equal(a, b) and torch.equal(la, lb)
     assert torch.equal(a, c) and torch.equal(la, lc)
+    assert torch.equal(a, e) and torch.equal(la, le)
 
 
 def test_head_dim_256_split_through_every_entry_point():

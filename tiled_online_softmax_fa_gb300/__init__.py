@@ -35,6 +35,7 @@ FA_KERNEL_ONE_TILE = 2  # 128 query rows per work unit; head dims 32 to 256
 FA_ORDER_AUTO = 0
 FA_ORDER_ONE_SNAKE = 1     # one snake over all work units
 FA_ORDER_GROUP_SNAKES = 2  # a snake per head group, odd groups mirrored
+FA_ORDER_SHIFTED_SNAKES = 3  # a snake per head group, each starting where the last left off
 
 
 class FwdOptions(ctypes.Structure):

@@ -224,6 +224,14 @@ int64_t unit_block(int64_t u, int64_t BH, int64_t nqb, int64_t gh) {
   return nqb - 1 - (u - g * gh * nqb) / heads;
 }
 
+// Order 2's per-group CTA offset: the CTAs a full group's part-filled last round used
+// (positions 0..rem-1 on an even round, G-rem..G-1 on an odd one) are skipped.
+int group_shift(int64_t group_items, int grid) {
+  const int64_t last = group_items / grid, rem = group_items % grid;
+  if (rem == 0) return 0;
+  return static_cast<int>((last & 1) ? grid - rem : rem);
+}
+
 // The busiest CTA's total cost when `items` items (costs cost(i), numbered as item_of
 // numbers them) are handed out over `grid` CTAs in item order `order` (item_of inverted:
 // item i of a group sits at round i / grid, position i % grid; order 0 is one group).
@@ -231,14 +239,17 @@ template <class Cost>
 double schedule_makespan(int64_t items, int grid, int order, int64_t group_items, Cost cost) {
   double load[kModelMaxSms] = {};
   const int64_t span = order == 0 ? items : group_items;
+  const int shift = group_shift(group_items, grid);
   int64_t g = 0;
   for (int64_t base = 0; base < items; base += span, ++g) {
     const int64_t n = std::min(span, items - base);
+    const int off = static_cast<int>(g * shift % grid);
     for (int64_t i = 0; i < n; ++i) {
       const int64_t k = i / grid;
       const int r = static_cast<int>(i - k * grid);
       const int c = (k & 1) ? grid - 1 - r : r;
-      load[(g & 1) ? grid - 1 - c : c] += cost(base + i);
+      const int cta = order == 1 ? ((g & 1) ? grid - 1 - c : c) : order == 2 ? (c + off) % grid : c;
+      load[cta] += cost(base + i);
     }
   }
   return *std::max_element(load, load + grid);
@@ -316,11 +327,13 @@ int schedule_order(int kernel, int64_t BH, int64_t N, int64_t d, int causal, int
         return e.order;
   }
   const CostModel& cm = cost_model(d) ? *cost_model(d) : kCostD128;
-  double t[2];
-  for (int o = 0; o < 2; ++o)
+  double t[3];
+  for (int o = 0; o < 3; ++o)
     t[o] = kernel == FA_KERNEL_ONE_TILE ? model_one_tile(cm, BH, N, d, causal, grid, o, splits)
                                          : model_two_tile(cm, BH, N, d, causal, grid, splits, o);
-  const int order = t[1] < t[0] ? 1 : 0;
+  int order = 0;
+  for (int o = 1; o < 3; ++o)
+    if (t[o] < t[order]) order = o;
   std::lock_guard<std::mutex> lock(g_order_mu);
   g_order_cache[g_order_next] = {BH, N, d, causal, grid, splits, kernel, order, true};
   g_order_next = (g_order_next + 1) % 32;
@@ -354,7 +367,7 @@ Plan plan_for(int64_t BH, int64_t N, int64_t d, int causal, int sms, int max_spl
     const int64_t items = (kernel == FA_KERNEL_ONE_TILE ? units1 : units) * splits;
     const int grid = static_cast<int>(std::min<int64_t>(sms, items));
     double t = 0.0;
-    for (int o = 0; o < 2; ++o) {
+    for (int o = 0; o < 3; ++o) {
       const double to = kernel == FA_KERNEL_ONE_TILE
                             ? model_one_tile(*cm, BH, N, d, causal, grid, o, splits)
                             : model_two_tile(*cm, BH, N, d, causal, grid, splits, o);
@@ -442,6 +455,7 @@ fa_sm103::Params base_params(void* o, float* lse, int64_t BH, int64_t N, int64_t
 void set_schedule(fa_sm103::Params& p, int grid, int order) {
   p.order = order;
   p.group_items = p.group_heads * p.nqb * p.splits;
+  p.group_shift = group_shift(p.group_items, grid);
   if (order == 0) {
     p.rounds_per_group = 0;
     p.num_rounds = (p.num_items + grid - 1) / grid;
@@ -457,6 +471,7 @@ int pick_order(const fa_fwd_options* opts, int kernel, int64_t BH, int64_t N, in
                int grid, int splits) {
   if (opts && opts->order == FA_ORDER_ONE_SNAKE) return 0;
   if (opts && opts->order == FA_ORDER_GROUP_SNAKES) return 1;
+  if (opts && opts->order == FA_ORDER_SHIFTED_SNAKES) return 2;
   return schedule_order(kernel, BH, N, d, causal, grid, splits);
 }
 
@@ -637,7 +652,7 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (lse && overlaps(lse, lse_bytes, o, bytes)) return set_error(FA_ERR_INVALID_ARG, "lse overlaps o");
   if (opts && (opts->wait_budget_cycles < 0 || opts->inject_skip_kv_load < 0 || opts->max_ctas < 0))
     return set_error(FA_ERR_INVALID_ARG, "negative option");
-  if (opts && (opts->order < FA_ORDER_AUTO || opts->order > FA_ORDER_GROUP_SNAKES))
+  if (opts && (opts->order < FA_ORDER_AUTO || opts->order > FA_ORDER_SHIFTED_SNAKES))
     return set_error(FA_ERR_INVALID_ARG, "unknown item order");
   if (kernel < FA_KERNEL_AUTO || kernel > FA_KERNEL_ONE_TILE)
     return set_error(FA_ERR_INVALID_ARG, "unknown kernel");
@@ -750,9 +765,8 @@ int fa_fwd_plan(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int allo
     const int64_t rows = pl.kernel == FA_KERNEL_ONE_TILE ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
     const int64_t items = (N + rows - 1) / rows * B * H * pl.splits;
     const int grid = static_cast<int>(std::min<int64_t>(sms, items));
-    *order = schedule_order(pl.kernel, B * H, N, d, causal, grid, pl.splits) == 1
-                 ? FA_ORDER_GROUP_SNAKES
-                 : FA_ORDER_ONE_SNAKE;
+    const int o = schedule_order(pl.kernel, B * H, N, d, causal, grid, pl.splits);
+    *order = o == 1 ? FA_ORDER_GROUP_SNAKES : o == 2 ? FA_ORDER_SHIFTED_SNAKES : FA_ORDER_ONE_SNAKE;
   }
   return FA_OK;
 }

@@ -79,7 +79,8 @@ struct Params {
   int splits;         // KV ranges per unit (1 = no split)
   int num_items;      // num_units * splits
   int group_heads;    // heads whose units are interleaved (K/V of a group fit in L2)
-  int order;          // item order over the grid: 0 one snake, 1 a snake per head group
+  int order;          // item order over the grid: 0 one snake, 1 / 2 a snake per head group
+  int group_shift;    // order 2: CTA offset added per group (mod gridDim.x)
   int group_items;    // items of a full head group (group_heads * nqb * splits)
   int rounds_per_group;  // order 1: ceil(group_items / gridDim.x)
   int num_rounds;     // rounds every role iterates over
@@ -122,6 +123,9 @@ __device__ __forceinline__ void unit_coords(int u, const Params& p, int& bh, int
 //   order 1: that snake restarted in every head group, with the CTA order mirrored in
 //            odd groups, so the CTAs that took the light end of one group's last round
 //            take the heaviest items of the next.  Each group then balances by itself.
+//   order 2: the snake restarted in every head group, group g's positions shifted by
+//            g * group_shift CTAs: each group starts right after the CTAs that took its
+//            predecessor's part-filled last round (all full groups fill that round alike).
 __device__ __forceinline__ int item_of(int k, const Params& p) {
   const int G = static_cast<int>(gridDim.x), c0 = static_cast<int>(blockIdx.x);
   if (p.order == 0) {
@@ -129,7 +133,13 @@ __device__ __forceinline__ int item_of(int k, const Params& p) {
     return i < p.num_items ? i : -1;
   }
   const int g = k / p.rounds_per_group, kg = k - g * p.rounds_per_group;
-  const int c = (g & 1) ? G - 1 - c0 : c0;
+  int c;
+  if (p.order == 1) {
+    c = (g & 1) ? G - 1 - c0 : c0;
+  } else {
+    c = c0 - static_cast<int>(static_cast<long long>(g) * p.group_shift % G);
+    if (c < 0) c += G;
+  }
   const int i = kg * G + ((kg & 1) ? G - 1 - c : c);
   const int base = g * p.group_items;
   const int n = p.num_items - base < p.group_items ? p.num_items - base : p.group_items;
