@@ -137,7 +137,9 @@ __device__ __forceinline__ int item_of(int k, const Params& p) {
   if (p.order == 1) {
     c = (g & 1) ? G - 1 - c0 : c0;
   } else {
-    c = c0 - static_cast<int>(static_cast<long long>(g) * p.group_shift % G);
+    // 32-bit arithmetic only: (g mod G) * group_shift < G^2 (G <= 1024 CTAs); a 64-bit
+    // remainder here compiles to a subroutine call in every role's loop
+    c = c0 - ((g % G) * p.group_shift) % G;
     if (c < 0) c += G;
   }
   const int i = kg * G + ((kg & 1) ? G - 1 - c : c);
