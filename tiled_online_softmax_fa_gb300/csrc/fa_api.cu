@@ -184,7 +184,8 @@ struct CostModel {
 };
 // Fitted to GB300 timings.  Unit and step costs: at d = 128, 82 two-vs-one pairs over 44
 // shapes (B 1-2, H 1-64, N 256-65536, causal and not); at d = 64 and 32, 88 pairs over
-// the same shapes; the model picks the faster kernel in all but one near-tie (0.4 %).
+// the same shapes; the model picks the faster kernel in all but two near-ties (0.1 and
+// 0.4 %).
 // Split costs: one to eight heads at N = 4096-32768 (16 shapes per head dim), each timed
 // on both kernels unsplit and split 2-8 ways; the model's pick is within 0.1 % of the
 // measured best at d = 32, 64 and 256 and within 8 % at d = 128 (one 406-vs-438 TFLOP/s
@@ -196,7 +197,7 @@ constexpr int kModelMaxSms = 1024;
 constexpr int64_t kModelUnitsPerSm = 4;      // more 256-row units per SM: two-tile kernel
 constexpr int64_t kModelMaxItems = 1 << 16;  // bound on the replayed schedule's length
 
-// The cost table of a head dim both kernels serve, else null.
+// The cost table of a head dim the planner models (32-256), else null (16: two-tile only).
 const CostModel* cost_model(int64_t d) {
   if (d == 256) return &kCostD256;
   if (d == 128) return &kCostD128;
@@ -297,12 +298,14 @@ double model_one_tile(const CostModel& cm, int64_t BH, int64_t N, int64_t d, int
   return t;
 }
 
-// The item order (Params::order) with the shorter modelled makespan for a launch of
-// `kernel` on `grid` CTAs.  The orders differ only with two or more head groups: one
-// snake over everything balances best when every group spans many rounds (b8 h32
-// S8192: 54 rounds); a snake per group wins when groups end in part-filled rounds (b1
-// h32 S8192, two groups of 3.4 rounds: 1154 -> 1266 TFLOP/s on GB300).  Decisions are
-// kept in a small cache, so repeated shapes replay the schedule once.
+// The item order (Params::order) with the shortest modelled makespan for a launch of
+// `kernel` on `grid` CTAs.  The orders differ only with two or more head groups.  One
+// snake over everything starts each group mid-round; a snake per group fixes that (b1
+// h32 S8192, two groups of 3.4 rounds: 1154 -> 1266 TFLOP/s on GB300), mirrored in odd
+// groups (best with two groups) or shifted past each predecessor's part-filled last
+// round (best with many: b8 h32 S16384 +1.4 %, d256 b4 h16 S8192 1554 TFLOP/s with each
+// group's K and V together in L2).  Decisions are kept in a small cache, so repeated
+// shapes replay the schedules once.
 constexpr int64_t kOrderMaxItems = int64_t{1} << 20;
 struct OrderEntry {
   int64_t BH, N, d;
