@@ -116,3 +116,30 @@ def test_pinned_kernel_needs_an_explicit_split_count():
         fa.fa_fwd_splitkv(q, q, q, causal=True, splits=0, options=fa.FwdOptions(kernel=ONE),
                           workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
     assert e.value.status == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_guard_regions_untouched(d):
+    """Canaries around o, lse and the workspace: the split kernel and the merge write
+    exactly [B, H, N, d], [B, H, N] and the workspace the pieces need (one-tile items
+    hold 128 rows, fewer than the 256-row sizing, so the tail of the sized workspace is
+    not written either way, and the canary past it must survive)."""
+    B, H, N, splits = 1, 3, 333, 3
+    q, k, v = (t.cuda() for t in workloads.make_inputs(W["n1k"], B=B, H=H, N=N, d=d, seed=11))
+    pad = 4096
+    obuf = torch.full((pad + B * H * N * d + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((pad + B * H * N + pad,), -3.0, dtype=torch.float32, device="cuda")
+    need = fa.splitkv_workspace_bytes(B, H, N, d, splits)
+    wbuf = torch.full((pad + need + pad,), 0xA5, dtype=torch.uint8, device="cuda")
+    o = obuf[pad:pad + B * H * N * d].view(B, H, N, d)
+    lse = lbuf[pad:pad + B * H * N].view(B, H, N)
+    fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, causal=True, splits=splits,
+                      workspace=wbuf[pad:pad + need], options=fa.FwdOptions(kernel=ONE))
+    assert fa.get_device_status() == fa.FA_OK
+    assert torch.all(obuf[:pad] == 7.0) and torch.all(obuf[-pad:] == 7.0)
+    assert torch.all(lbuf[:pad] == -3.0) and torch.all(lbuf[-pad:] == -3.0)
+    assert torch.all(wbuf[:pad] == 0xA5) and torch.all(wbuf[-pad:] == 0xA5)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    ref, lref = fa.fa_fwd(q, k, v, causal=True, options=fa.FwdOptions(kernel=ONE))
+    assert (o.float() - ref.float()).abs().max() <= 8e-3
+    assert (lse - lref).abs().max() <= 1e-3
