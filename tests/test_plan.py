@@ -267,3 +267,46 @@ def test_order_is_reported_for_every_plan():
         for B, H, N in [(1, 20, 8192), (8, 32, 2048), (1, 3, 100)]:
             k, s, o = fa.fwd_plan(B, H, N, d, False, allow_split=True, with_order=True, num_sms=SMS)
             assert o in (fa.FA_ORDER_ONE_SNAKE, fa.FA_ORDER_GROUP_SNAKES, fa.FA_ORDER_SHIFTED_SNAKES)
+
+
+# --- invariants over many shapes --------------------------------------------------------
+def _shapes(n=300, seed=2024):
+    import random
+    rng = random.Random(seed)
+    for _ in range(n):
+        B = rng.choice([1, 1, 1, 2, 4, 8])
+        H = rng.choice([1, 2, 3, 4, 5, 8, 12, 16, 20, 32, 48, 64])
+        N = rng.choice([1, 100, 128, 129, 255, 256, 300, 1000, 2048, 4096, 6000, 8192, 12288,
+                        16384, 32768, 65536])
+        d = rng.choice([16, 32, 64, 128, 256])
+        yield B, H, N, d, rng.random() < 0.8
+
+
+def test_every_plan_is_a_launch_the_library_can_run():
+    orders = (fa.FA_ORDER_ONE_SNAKE, fa.FA_ORDER_GROUP_SNAKES, fa.FA_ORDER_SHIFTED_SNAKES)
+    for B, H, N, d, causal in _shapes():
+        for split in (False, True):
+            kernel, splits, order = fa.fwd_plan(B, H, N, d, causal, allow_split=split,
+                                                with_order=True, num_sms=SMS)
+            assert kernel in (TWO, ONE)
+            assert kernel != TWO or d <= 128, (B, H, N, d)   # the two-tile kernel: d <= 128
+            assert kernel != ONE or d >= 32, (B, H, N, d)    # the one-tile kernel: d >= 32
+            assert 1 <= splits <= 64 and (split or splits == 1)
+            assert order in orders
+            # the same answer again (the plan cache)
+            assert fa.fwd_plan(B, H, N, d, causal, allow_split=split, with_order=True,
+                               num_sms=SMS) == (kernel, splits, order)
+
+
+def test_workspace_sizing_covers_both_kernels_split_layouts():
+    # fa_splitkv_workspace_bytes sizes 256-row items (the two-tile kernel); the one-tile
+    # kernel's items hold 128 rows over ceil(N / 128) query blocks.  The library puts the
+    # partial outputs first and the partial lse after them, so both layouts must fit.
+    for B, H, N, d, _ in _shapes():
+        for splits in (2, 3, 8, 64):
+            need = fa.splitkv_workspace_bytes(B, H, N, d, splits)
+            one_tile = B * H * -(-N // 128) * splits * 128 * (d + 1) * 4
+            assert one_tile <= need, (B, H, N, d, splits)
+            if d <= 128:
+                two_tile = B * H * -(-N // 256) * splits * 256 * (d + 1) * 4
+                assert two_tile == need
