@@ -16,8 +16,9 @@
  * The logsumexp output is not on the pages; it is the plain definition above.
  *
  * All functions are plain C and take raw pointers and sizes.  Compute is asynchronous
- * on the caller's stream.  None allocates device memory, except that the first call of
- * fa_fwd_materialised on a device creates a cuBLAS handle (see there).
+ * on the caller's stream.  None allocates device memory, and the library links no BLAS:
+ * the materialised baseline (cuBLAS GEMMs, N x N matrices in device memory) is a
+ * separate library, declared in fa_baseline.h.
  *
  * CUDA graphs: fa_fwd, fa_fwd_opts, fa_fwd_splitkv and fa_fwd_splitkv_noalloc may be
  * captured into a graph on the caller's stream and replayed (the launch is planned at
@@ -248,34 +249,6 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 /* Size in bytes of the built-in scratch used by fa_fwd_splitkv_noalloc. */
 int64_t fa_noalloc_scratch_bytes(void);
 
-/*
- * fa_fwd_materialised -- the materialised baseline: the same result computed the way the
- * pages' `standard_attention` does it (aiml.sh "Speed up long contexts with
- * FlashAttention", lab.py), with the N x N matrices in device memory:
- *     S = scale * Q K^T            fp32 [B*H, N, N] in the workspace (cuBLAS batched GEMM)
- *     P = exp(S - row max) + mask  bf16 [B*H, N, N] in the workspace, with the row sums
- *                                  of the rounded P and lse = ln sum_j exp(s_j) (this
- *                                  library's row kernel; masked entries are 0)
- *     acc = P V                    fp32 [B*H, N, d] in the workspace (cuBLAS batched GEMM)
- *     O = acc / row sum            bf16 (this library's kernel)
- * It exists to measure the traffic and time the tiled kernels avoid (the pages model
- * 4 H N^2 elements of such traffic per batch); it is not a fast path.
- *
- *   workspace  device memory, 256-byte aligned, caller-owned, at least
- *              fa_materialised_workspace_bytes(B, H, N, d) (about 6 B H N^2 + 4 B H N d
- *              bytes); must not overlap any tensor.  Its contents on entry do not matter.
- * Other arguments and errors as fa_fwd (N up to 2^20 and B*H*N < 2^31 here).  Unlike the
- * other entry points, the first call on a device creates a cuBLAS handle for it (cuBLAS
- * allocates its own device workspace then); calls are serialised on a library lock.
- */
-int fa_fwd_materialised(const void* q, const void* k, const void* v, void* o, float* lse,
-                        int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
-                        void* workspace, size_t workspace_bytes, void* stream);
-
-/* Workspace bytes fa_fwd_materialised needs (S, P, acc and row sums, each rounded up to a
-   multiple of 256 bytes); -1 on bad or too large sizes or an unsupported head dim. */
-int64_t fa_materialised_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
-
 /* Static description of a status code. Never NULL. */
 const char* fa_strerror(int status);
 
@@ -291,6 +264,27 @@ int fa_get_device_status(void* stream);
 
 /* Library version, as major*10000 + minor*100 + patch. */
 int fa_version(void);
+
+/*
+ * fa_row_kernel_register_check -- the check every first launch of the two-tile kernel
+ * (fa_fwd_row_kernel, head dims 16-128) makes on its compiled register allocation, as a
+ * pure function (no CUDA call).  That kernel moves registers between its warpgroups with
+ * setmaxnreg: the softmax warpgroups raise their share while the epilogue and control
+ * warpgroups lower theirs, and the shares add up to exactly 512 threads x 128 registers.
+ * setmaxnreg waits, without any bound, until the block's pool can satisfy it, so a build
+ * compiled to another allocation (a different compiler release, -G, -maxrregcount) would
+ * hang the GPU.  The library therefore launches that kernel only when
+ * cudaFuncGetAttributes reports num_regs == 128 and max_threads_per_block >= 512.
+ * Returns FA_OK, or FA_ERR_UNSUPPORTED with the reason in fa_last_error().
+ */
+int fa_row_kernel_register_check(int num_regs, int max_threads_per_block);
+
+/*
+ * Test hook: while num_regs > 0, every launch of the two-tile kernel runs the check above
+ * with num_regs in place of the compiled count (and is refused when that fails, before
+ * anything is launched); 0 restores normal operation.  Process-wide; for tests only.
+ */
+void fa_test_override_kernel_registers(int num_regs);
 
 #ifdef __cplusplus
 }

@@ -1,8 +1,10 @@
-"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
-function ``include/fa.h`` declares, and rejects bad arguments before touching CUDA."""
+"""Host-side checks of the C ABI that need no GPU: both libraries load, each exports every
+function its header declares (``include/fa.h``: libfa_sm103.so, ``include/fa_baseline.h``:
+libfa_baseline.so), and they reject bad arguments before touching CUDA."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -11,15 +13,15 @@ import tiled_online_softmax_fa_gb300 as fa
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _declared_functions():
-    names = set()
-    inc = os.path.join(ROOT, "include")
-    for fn in os.listdir(inc):
-        if fn.endswith(".h"):
-            with open(os.path.join(inc, fn)) as f:
-                text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
-            names |= set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text))
-    return sorted(names)
+def _declared_functions(header):
+    with open(os.path.join(ROOT, "include", header)) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_header_belongs_to_a_library():
+    assert sorted(fn for fn in os.listdir(os.path.join(ROOT, "include")) if fn.endswith(".h")) == \
+        ["fa.h", "fa_baseline.h"]
 
 
 def test_library_builds_and_loads():
@@ -29,13 +31,59 @@ def test_library_builds_and_loads():
 
 
 def test_every_declared_symbol_is_exported():
-    names = _declared_functions()
+    names = _declared_functions("fa.h")
     assert {"fa_fwd", "fa_fwd_opts", "fa_strerror", "fa_last_error", "fa_get_device_status",
             "fa_version", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes",
-            "fa_splitkv_auto_splits"} <= set(names)
+            "fa_splitkv_auto_splits", "fa_row_kernel_register_check"} <= set(names)
     lib = fa.load_library()
     for name in names:
         assert hasattr(lib, name), name
+    base = _declared_functions("fa_baseline.h")
+    assert set(base) == {"fa_fwd_materialised", "fa_materialised_workspace_bytes",
+                         "fa_baseline_last_error"}
+    blib = fa.load_baseline_library()
+    for name in base:
+        assert hasattr(blib, name), name
+
+
+def _needed(path):
+    out = subprocess.run(["readelf", "-d", path], capture_output=True, text=True, check=True).stdout
+    return re.findall(r"\(NEEDED\)\s+Shared library: \[([^\]]+)\]", out)
+
+
+def test_forward_library_links_no_blas():
+    from tiled_online_softmax_fa_gb300 import build
+    fa.load_library()
+    fa.load_baseline_library()
+    assert not any("cublas" in n for n in _needed(build.LIB_PATH)), _needed(build.LIB_PATH)
+    assert any("cublas" in n for n in _needed(build.BASELINE_LIB_PATH))
+    # and it exports none of the baseline's entry points
+    assert not hasattr(fa.load_library(), "fa_fwd_materialised")
+
+
+def test_register_split_check():
+    # the allocation the two-tile kernel's setmaxnreg split is written for
+    assert fa.row_kernel_register_check(128, 512) == fa.FA_OK
+    assert fa.last_error() == ""
+    # anything else would leave setmaxnreg.inc waiting forever: refused
+    for regs, threads in ((120, 512), (96, 512), (127, 1024), (168, 384), (128, 384), (0, 512)):
+        assert fa.row_kernel_register_check(regs, threads) == fa.FA_ERR_UNSUPPORTED
+        assert "setmaxnreg" in fa.last_error()
+
+
+def test_build_rejects_other_register_counts():
+    from tiled_online_softmax_fa_gb300 import build
+    name = "_ZN8fa_sm1034rowk17fa_fwd_row_kernelILi128ELb0EEEv14CUtensorMap_stS2_S2_NS_6ParamsE"
+    log = (f"ptxas info    : Compiling entry function '{name}' for 'sm_103a'\n"
+           f"ptxas info    : Function properties for {name}\n"
+           "    0 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads\n"
+           "ptxas info    : Used {regs} registers, used 1 barriers, 6400 bytes smem\n")
+    build.check_row_kernel_registers(log.format(regs=128))
+    assert build.kernel_registers(log.format(regs=120)) == {name: 120}
+    with pytest.raises(RuntimeError, match="setmaxnreg"):
+        build.check_row_kernel_registers(log.format(regs=120))
+    with pytest.raises(RuntimeError, match="no fa_fwd_row_kernel"):
+        build.check_row_kernel_registers("")
 
 
 def test_strerror_covers_every_status():
@@ -104,6 +152,11 @@ def test_splitkv_workspace_bytes():
     assert fa.splitkv_workspace_bytes(1, 32, 1024, 256, 1) == 0
     # head dim 256 splits on the one-tile kernel: 128-row items, the same total rows
     assert fa.splitkv_workspace_bytes(1, 32, 1024, 256, 4) == units * 4 * 256 * (256 + 1) * 4
+    # sizes beyond the kernels' 32-bit indices: -1, never a wrapped (small) byte count
+    assert fa.splitkv_workspace_bytes(1 << 20, 1 << 12, 1, 128, 2) == -1   # B*H > 2^31
+    assert fa.splitkv_workspace_bytes(1, 1, (1 << 30) + 1, 128, 2) == -1    # N > 2^30
+    assert fa.splitkv_workspace_bytes(1 << 15, 1 << 15, 1 << 14, 128, 64) == -1  # units
+    assert fa.splitkv_workspace_bytes(1 << 14, 1 << 10, 1 << 10, 128, 64) == -1  # items
 
 
 def _split(**kw):
@@ -160,9 +213,22 @@ def _mat(**kw):
 ])
 def test_materialised_argument_errors(kw, want):
     assert _mat(**kw) == want
-    assert fa.last_error() != ""
+    assert fa.load_baseline_library().fa_baseline_last_error().decode() != ""
 
 
 def test_materialised_empty_is_a_noop():
     assert _mat(B=0) == fa.FA_OK
     assert _mat(N=0, ws_ptr=0) == fa.FA_OK
+
+
+@pytest.mark.parametrize("B,H,N,splits", [
+    (1 << 15, 1 << 15, 1 << 14, 2),    # work units beyond int32
+    (1 << 14, 1 << 10, 1 << 10, 64),   # units x splits beyond int32
+    (1 << 20, 1 << 12, 128, 2),        # B*H beyond int32
+])
+def test_noalloc_range_checks_come_before_any_size_arithmetic(B, H, N, splits):
+    # rejected on the host, before planning or sizing the scratch (no CUDA call needed)
+    rc = fa.fa_fwd_splitkv_noalloc_raw(0x10000, 0x20000, 0x30000, 0x40000, 0, B, H, N, 128,
+                                       True, 0.088, splits)
+    assert rc == fa.FA_ERR_UNSUPPORTED
+    assert fa.last_error() != ""

@@ -1,9 +1,11 @@
 """Python binding of the GB300 (sm_103a) attention forward library.
 
-Argument marshalling only: every step of the computation runs in the CUDA kernel
-behind the C ABI of ``include/fa.h``.  PyTorch supplies device memory and the
-stream.  There is no fallback: if the compiled library cannot be loaded, every
-call raises.
+Argument marshalling only: every step of the computation runs in the CUDA kernels
+behind the C ABI of ``include/fa.h`` (libfa_sm103.so).  The materialised baseline,
+``fa_fwd_materialised``, lives in a separate library (``include/fa_baseline.h``,
+libfa_baseline.so, linked with cuBLAS) loaded only when it is called.  PyTorch supplies
+device memory and the stream.  There is no fallback: if a compiled library cannot be
+loaded, every call into it raises.
 """
 from __future__ import annotations
 
@@ -17,7 +19,8 @@ __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_splitkv", "fa_fwd_splitkv_raw",
            "splitkv_workspace_bytes", "splitkv_auto_splits", "fa_fwd_splitkv_noalloc_raw",
            "noalloc_scratch_bytes", "fa_fwd_materialised", "fa_fwd_materialised_raw",
            "materialised_workspace_bytes", "get_device_status", "strerror", "last_error", "version",
-           "load_library", "FAError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED",
+           "load_library", "load_baseline_library", "row_kernel_register_check",
+           "override_kernel_registers_for_test", "FAError", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED",
            "FA_ERR_MISALIGNED", "FA_ERR_ARCH", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
            "FwdOptions", "SUPPORTED_HEAD_DIMS"]
 
@@ -55,7 +58,16 @@ class FAError(RuntimeError):
                          + (f": {detail}" if detail else ""))
 
 
+class BaselineError(FAError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = load_baseline_library().fa_baseline_last_error().decode()
+        RuntimeError.__init__(self, f"{where}: {strerror(status)} (status {status})"
+                              + (f": {detail}" if detail else ""))
+
+
 _lib = None
+_baseline_lib = None
 _lock = threading.Lock()
 
 
@@ -101,13 +113,44 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
         lib.fa_noalloc_scratch_bytes.argtypes = []
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_int64
+        lib.fa_row_kernel_register_check.argtypes = [ctypes.c_int, ctypes.c_int]
+        lib.fa_row_kernel_register_check.restype = ctypes.c_int
+        lib.fa_test_override_kernel_registers.argtypes = [ctypes.c_int]
+        lib.fa_test_override_kernel_registers.restype = None
+        _lib = lib
+        return lib
+
+
+def load_baseline_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libfa_baseline.so (materialised path)."""
+    global _baseline_lib
+    with _lock:
+        if _baseline_lib is not None:
+            return _baseline_lib
+        if build_if_missing:
+            _build.build()
+        lib = ctypes.CDLL(_build.BASELINE_LIB_PATH)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
         lib.fa_fwd_materialised.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int,
                                             ctypes.c_float, vp, ctypes.c_size_t, vp]
         lib.fa_fwd_materialised.restype = ctypes.c_int
         lib.fa_materialised_workspace_bytes.argtypes = [i64, i64, i64, i64]
         lib.fa_materialised_workspace_bytes.restype = ctypes.c_int64
-        _lib = lib
+        lib.fa_baseline_last_error.argtypes = []
+        lib.fa_baseline_last_error.restype = ctypes.c_char_p
+        _baseline_lib = lib
         return lib
+
+
+def row_kernel_register_check(num_regs: int, max_threads_per_block: int) -> int:
+    """The two-tile kernel's launch check on its compiled register allocation (pure)."""
+    return int(load_library().fa_row_kernel_register_check(int(num_regs), int(max_threads_per_block)))
+
+
+def override_kernel_registers_for_test(num_regs: int) -> None:
+    """Test hook: launches of the two-tile kernel check `num_regs` instead of the compiled
+    register count while it is > 0; 0 restores normal operation."""
+    load_library().fa_test_override_kernel_registers(int(num_regs))
 
 
 def strerror(status: int) -> str:
@@ -270,13 +313,13 @@ def noalloc_scratch_bytes() -> int:
 
 
 def materialised_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
-    return int(load_library().fa_materialised_workspace_bytes(B, H, N, d))
+    return int(load_baseline_library().fa_materialised_workspace_bytes(B, H, N, d))
 
 
 def fa_fwd_materialised_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal, scale,
                             ws_ptr, ws_bytes, stream: int = 0) -> int:
     """Call fa_fwd_materialised with raw device addresses; returns the status code."""
-    lib = load_library()
+    lib = load_baseline_library()
     return int(lib.fa_fwd_materialised(q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None,
                                        lse_ptr or None, int(B), int(H), int(N), int(d),
                                        int(bool(causal)), float(scale), ws_ptr or None,
@@ -304,7 +347,7 @@ def fa_fwd_materialised(q, k, v, o=None, lse=None, causal: bool = True,
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     need = materialised_workspace_bytes(B, H, N, d)
     if need < 0:
-        raise FAError(FA_ERR_UNSUPPORTED, "fa_fwd_materialised")
+        raise BaselineError(FA_ERR_UNSUPPORTED, "fa_fwd_materialised")
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = fa_fwd_materialised_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
@@ -312,7 +355,7 @@ def fa_fwd_materialised(q, k, v, o=None, lse=None, causal: bool = True,
                                  workspace.numel() * workspace.element_size(),
                                  _stream_handle(stream, q.device))
     if rc != FA_OK:
-        raise FAError(rc, "fa_fwd_materialised")
+        raise BaselineError(rc, "fa_fwd_materialised")
     return o, lse
 
 

@@ -1,10 +1,10 @@
 // fa_api.cu -- host side of the C ABI declared in include/fa.h: argument checks, TMA
 // tensor-map encoding, the persistent launch and the device status word.
-#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -16,7 +16,6 @@
 #include "fa_fwd_1tile_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_fwd_row_kernel.cuh"
-#include "fa_materialised_kernel.cuh"
 #include "fa_merge_kernel.cuh"
 
 // Built-in scratch for fa_fwd_splitkv_noalloc: callers that may not allocate device
@@ -484,6 +483,42 @@ int grid_for(const DeviceState& dev, const fa_fwd_options* opts, int items) {
   return grid > items ? items : grid;
 }
 
+// ---- register split of the two-tile kernel ------------------------------------------
+// fa_fwd_row_kernel moves registers between its warpgroups with setmaxnreg (softmax up,
+// epilogue and control down); the shares add up to exactly the registers the block is
+// launched with, 512 threads x kLaunchRegs.  setmaxnreg.inc waits until the block's pool
+// can satisfy it, and that wait has no bound: a build whose per-thread allocation differs
+// (another compiler release, -G, -maxrregcount) would leave the softmax warpgroups waiting
+// forever, outside every bounded barrier wait of the kernel.  So the compiled allocation
+// is checked before the first launch, and a mismatch refuses the launch.
+std::atomic<int> g_regs_override{0};  // test hook: > 0 stands in for the compiled count
+
+int register_split_check(int num_regs, int max_threads) {
+  using namespace fa_sm103::rowk;
+  if (num_regs == kLaunchRegs && max_threads >= kThreadsR) return FA_OK;
+  char buf[240];
+  snprintf(buf, sizeof buf,
+           "fa_fwd_row_kernel was compiled to %d registers per thread (at most %d threads per "
+           "block); its setmaxnreg split needs exactly %d with %d threads, so it is not launched",
+           num_regs, max_threads, kLaunchRegs, kThreadsR);
+  return set_error(FA_ERR_UNSUPPORTED, buf);
+}
+
+template <int HD>
+int check_row_kernel_registers() {
+  const void* fns[2] = {reinterpret_cast<const void*>(fa_sm103::rowk::fa_fwd_row_kernel<HD, false>),
+                        reinterpret_cast<const void*>(fa_sm103::rowk::fa_fwd_row_kernel<HD, true>)};
+  for (const void* fn : fns) {
+    cudaFuncAttributes a;
+    const cudaError_t e = cudaFuncGetAttributes(&a, fn);
+    if (e != cudaSuccess) return cuda_error("cudaFuncGetAttributes", e);
+    const int fake = g_regs_override.load();
+    const int st = register_split_check(fake > 0 ? fake : a.numRegs, a.maxThreadsPerBlock);
+    if (st != FA_OK) return st;
+  }
+  return FA_OK;
+}
+
 template <int HD>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
            int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
@@ -491,6 +526,9 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   using C = fa_sm103::Cfg<HD>;
   CUtensorMap mq, mk, mv;
   int st;
+  // the first launch per device and head dim (and every launch while the test hook is set)
+  if ((!smem_set || g_regs_override.load() > 0) && (st = check_row_kernel_registers<HD>()) != FA_OK)
+    return st;
   if ((st = encode_map(&mq, q, BH, N, HD)) != FA_OK) return st;
   if ((st = encode_map(&mk, k, BH, N, HD)) != FA_OK) return st;
   if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
@@ -611,6 +649,27 @@ int device_state(DeviceState** out) {
   return FA_OK;
 }
 
+// Range checks every entry point applies before any size arithmetic (B, H, N > 0, d a
+// supported head dim): B*H, N and the work units fit the kernels' 32-bit indices, and
+// the tensors' byte counts fit int64.
+int check_ranges(int64_t B, int64_t H, int64_t N, int64_t d) {
+  if (B > INT32_MAX / H) return set_error(FA_ERR_UNSUPPORTED, "B*H too large");
+  const int64_t BH = B * H;
+  if (N > (int64_t{1} << 30)) return set_error(FA_ERR_UNSUPPORTED, "N too large");
+  // head dims 32 to 256 may run the one-tile kernel's 128-row units
+  const int64_t unit_rows = d >= 32 ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
+  if (((N + unit_rows - 1) / unit_rows) * BH > INT32_MAX)
+    return set_error(FA_ERR_UNSUPPORTED, "too many work units");
+  if (BH > (INT64_MAX / 4) / (N * d)) return set_error(FA_ERR_UNSUPPORTED, "tensor too large");
+  return FA_OK;
+}
+
+// A launch's items (units x key-range pieces) index the kernels' schedule as int.
+bool items_fit(int64_t BH, int64_t N, int kernel, int splits) {
+  const int64_t rows = kernel == FA_KERNEL_ONE_TILE ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
+  return ((N + rows - 1) / rows) * BH * splits <= INT32_MAX;
+}
+
 }  // namespace
 
 namespace {
@@ -632,14 +691,9 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (!q || !k || !v || !o) return set_error(FA_ERR_INVALID_ARG, "null tensor pointer");
   if (!std::isfinite(scale) || scale < 0.f)
     return set_error(FA_ERR_INVALID_ARG, "scale must be finite and >= 0");
-  if (B > INT32_MAX / H) return set_error(FA_ERR_UNSUPPORTED, "B*H too large");
+  int st = check_ranges(B, H, N, d);
+  if (st != FA_OK) return st;
   const int64_t BH = B * H;
-  if (N > (int64_t{1} << 30)) return set_error(FA_ERR_UNSUPPORTED, "N too large");
-  // head dims 32 to 256 may run the one-tile kernel's 128-row units
-  const int64_t unit_rows = d >= 32 ? fa_sm103::one::kUnitRows1 : fa_sm103::kUnitRows;
-  const int64_t units = ((N + unit_rows - 1) / unit_rows) * BH;
-  if (units > INT32_MAX) return set_error(FA_ERR_UNSUPPORTED, "too many work units");
-  if (BH > (INT64_MAX / 4) / (N * d)) return set_error(FA_ERR_UNSUPPORTED, "tensor too large");
   const size_t bytes = static_cast<size_t>(BH * N * d) * 2;
   const size_t lse_bytes = static_cast<size_t>(BH * N) * 4;
   for (const void* ptr : {q, k, v, static_cast<const void*>(o)})
@@ -676,7 +730,7 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
 
   // ---- device checks ----
   DeviceState* dev = nullptr;
-  int st = device_state(&dev);
+  st = device_state(&dev);
   if (st != FA_OK) return st;
   if (!dev->arch_ok) return set_error(FA_ERR_ARCH, "device is not sm_103 (GB300-class)");
   if (splits == 0) {
@@ -696,6 +750,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
              : d == 256  ? static_cast<int>(FA_KERNEL_ONE_TILE)
                          : static_cast<int>(FA_KERNEL_TWO_TILE);
   }
+  if (!items_fit(BH, N, kernel, splits))
+    return set_error(FA_ERR_UNSUPPORTED, "too many work items (units x splits)");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kernel == FA_KERNEL_ONE_TILE) {
     bool& set_one = dev->smem_set_one[hd];
@@ -730,6 +786,10 @@ int64_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, i
   if (B < 0 || H < 0 || N < 0 || head_dim_index(d) < 0 || splits < 1 || splits > kMaxSplits)
     return -1;
   if (B == 0 || H == 0 || N == 0) return 0;
+  if (check_ranges(B, H, N, d) != FA_OK) return -1;
+  // the two-tile kernel's 256-row items are the larger count of rows; both kernels' items
+  // must fit the schedule's int index
+  if (!items_fit(B * H, N, FA_KERNEL_ONE_TILE, splits)) return -1;
   return workspace_bytes(B * H, N, d, splits);
 }
 
@@ -838,10 +898,12 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   if (head_dim_index(d) < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64, 128 or 256");
   if (splits < 0 || splits > kMaxSplits) return set_error(FA_ERR_INVALID_ARG, "splits must be in [0, 64]");
   if (B == 0 || H == 0 || N == 0) return FA_OK;
-  if (B > INT32_MAX / H || N > (int64_t{1} << 30))
-    return set_error(FA_ERR_UNSUPPORTED, "sizes beyond the kernel's range");
+  int st = check_ranges(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (splits > 1 && !items_fit(B * H, N, FA_KERNEL_ONE_TILE, splits))
+    return set_error(FA_ERR_UNSUPPORTED, "too many work items (units x splits)");
   DeviceState* dev = nullptr;
-  int st = device_state(&dev);
+  st = device_state(&dev);
   if (st != FA_OK) return st;
   int kernel = FA_KERNEL_AUTO;
   if (splits == 0) {
@@ -869,126 +931,7 @@ int64_t fa_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kStaticScra
 
 }  // extern "C"
 
-// ------------------------------------------------------------------------------------
-// Materialised baseline: S = scale Q K^T (fp32) and P = softmax(S) (bf16) in HBM, O = P V.
-// ------------------------------------------------------------------------------------
-namespace {
-
-cublasHandle_t g_cublas[kMaxDevices];
-
-// Workspace layout: S fp32 [BH, N, N] | P bf16 [BH, N, N] | acc fp32 [BH, N, d] |
-// l_round fp32 [BH, N] (each part starts on a 256-byte boundary).
-int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
-int64_t materialised_bytes(int64_t BH, int64_t N, int64_t d) {
-  return round256(BH * N * N * 4) + round256(BH * N * N * 2) + round256(BH * N * d * 4) +
-         round256(BH * N * 4);
-}
-
-int cublas_error(const char* what, cublasStatus_t st) {
-  char buf[96];
-  snprintf(buf, sizeof buf, "%s failed (cublasStatus %d)", what, static_cast<int>(st));
-  return set_error(FA_ERR_CUDA, buf);
-}
-
-}  // namespace
-
 extern "C" {
-
-int64_t fa_materialised_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d) {
-  if (B < 0 || H < 0 || N < 0 || head_dim_index(d) < 0) return -1;
-  if (B == 0 || H == 0 || N == 0) return 0;
-  if (B > INT32_MAX / H || N > (int64_t{1} << 20)) return -1;
-  const int64_t BH = B * H;
-  if (BH > (INT64_MAX / 8) / (N * N)) return -1;
-  return materialised_bytes(BH, N, d);
-}
-
-int fa_fwd_materialised(const void* q, const void* k, const void* v, void* o, float* lse,
-                        int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
-                        void* workspace, size_t workspace_bytes_given, void* stream) {
-  t_last_error.clear();
-  if (B < 0 || H < 0 || N < 0) return set_error(FA_ERR_INVALID_ARG, "negative size");
-  if (head_dim_index(d) < 0) return set_error(FA_ERR_UNSUPPORTED, "head dim must be 16, 32, 64, 128 or 256");
-  if (B == 0 || H == 0 || N == 0) return FA_OK;
-  if (!q || !k || !v || !o) return set_error(FA_ERR_INVALID_ARG, "null tensor pointer");
-  if (!std::isfinite(scale) || scale < 0.f)
-    return set_error(FA_ERR_INVALID_ARG, "scale must be finite and >= 0");
-  const int64_t need = fa_materialised_workspace_bytes(B, H, N, d);
-  if (need < 0) return set_error(FA_ERR_UNSUPPORTED, "sizes beyond the materialised path's range");
-  const int64_t BH = B * H;
-  if (BH * N > INT32_MAX) return set_error(FA_ERR_UNSUPPORTED, "too many rows for the softmax grid");
-  if (!workspace) return set_error(FA_ERR_INVALID_ARG, "the materialised path needs a workspace");
-  if (static_cast<int64_t>(workspace_bytes_given) < need)
-    return set_error(FA_ERR_INVALID_ARG, "workspace too small (see fa_materialised_workspace_bytes)");
-  for (const void* ptr : {q, k, v, static_cast<const void*>(o)})
-    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
-      return set_error(FA_ERR_MISALIGNED, "tensor base address not 16-byte aligned");
-  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
-    return set_error(FA_ERR_MISALIGNED, "workspace not 256-byte aligned");
-  if (lse && reinterpret_cast<uintptr_t>(lse) % 4 != 0)
-    return set_error(FA_ERR_MISALIGNED, "lse not 4-byte aligned");
-  const size_t bytes = static_cast<size_t>(BH * N * d) * 2;
-  const size_t lse_bytes = static_cast<size_t>(BH * N) * 4;
-  for (const void* in : {q, k, v}) {
-    if (overlaps(o, bytes, in, bytes)) return set_error(FA_ERR_INVALID_ARG, "o overlaps an input");
-    if (lse && overlaps(lse, lse_bytes, in, bytes))
-      return set_error(FA_ERR_INVALID_ARG, "lse overlaps an input");
-  }
-  if (lse && overlaps(lse, lse_bytes, o, bytes)) return set_error(FA_ERR_INVALID_ARG, "lse overlaps o");
-  for (const void* t : {q, k, v, static_cast<const void*>(o)})
-    if (overlaps(workspace, static_cast<size_t>(need), t, bytes))
-      return set_error(FA_ERR_INVALID_ARG, "workspace overlaps a tensor");
-  if (lse && overlaps(workspace, static_cast<size_t>(need), lse, lse_bytes))
-    return set_error(FA_ERR_INVALID_ARG, "workspace overlaps lse");
-
-  DeviceState* dev = nullptr;
-  int st = device_state(&dev);
-  if (st != FA_OK) return st;
-  if (!dev->arch_ok) return set_error(FA_ERR_ARCH, "device is not sm_103 (GB300-class)");
-  int dev_index = 0;
-  cudaError_t e = cudaGetDevice(&dev_index);
-  if (e != cudaSuccess) return cuda_error("cudaGetDevice", e);
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* S = reinterpret_cast<float*>(ws);
-  __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(ws + round256(BH * N * N * 4));
-  float* acc = reinterpret_cast<float*>(ws + round256(BH * N * N * 4) + round256(BH * N * N * 2));
-  float* l_round = reinterpret_cast<float*>(ws + round256(BH * N * N * 4) + round256(BH * N * N * 2) +
-                                            round256(BH * N * d * 4));
-  const int n = static_cast<int>(N), dd = static_cast<int>(d);
-  const long long sN2 = static_cast<long long>(N) * N, sNd = static_cast<long long>(N) * d;
-  const float one = 1.f, zero = 0.f;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // one handle per device; the lock also serialises its stream binding across host threads
-  std::lock_guard<std::mutex> lock(g_mu);
-  cublasHandle_t& h = g_cublas[dev_index];
-  cublasStatus_t cs;
-  if (!h && (cs = cublasCreate(&h)) != CUBLAS_STATUS_SUCCESS) {
-    h = nullptr;
-    return cublas_error("cublasCreate", cs);
-  }
-  if ((cs = cublasSetStream(h, s)) != CUBLAS_STATUS_SUCCESS) return cublas_error("cublasSetStream", cs);
-  // column-major view: S^T (N x N) = K (d x N)^T * Q (d x N), i.e. S[i][j] = scale q_i . k_j
-  cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, n, n, dd, &scale, k, CUDA_R_16BF, dd,
-                                  sNd, q, CUDA_R_16BF, dd, sNd, &zero, S, CUDA_R_32F, n, sN2,
-                                  static_cast<int>(BH), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (cs != CUBLAS_STATUS_SUCCESS) return cublas_error("cublasGemmStridedBatchedEx (S = Q K^T)", cs);
-  fa_sm103::mat::row_softmax_kernel<<<static_cast<unsigned>(BH * N), fa_sm103::mat::kRowThreads, 0,
-                                      s>>>(S, P, l_round, lse, n, causal ? 1 : 0);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error("row softmax launch", e);
-  // column-major view: acc^T (d x N) = V^T (d x N) * P^T (N x N), i.e. acc[i] = sum_j P[i][j] v_j
-  cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, dd, n, n, &one, v, CUDA_R_16BF, dd,
-                                  sNd, P, CUDA_R_16BF, n, sN2, &zero, acc, CUDA_R_32F, dd, sNd,
-                                  static_cast<int>(BH), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (cs != CUBLAS_STATUS_SUCCESS) return cublas_error("cublasGemmStridedBatchedEx (P V)", cs);
-  const int64_t quads = BH * N * d / 4;
-  fa_sm103::mat::normalise_kernel<<<static_cast<unsigned>((quads + 255) / 256), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(acc), l_round, static_cast<uint2*>(o), quads, dd);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error("normalise launch", e);
-  return FA_OK;
-}
 
 const char* fa_strerror(int status) {
   switch (status) {
@@ -1020,5 +963,14 @@ int fa_get_device_status(void* stream) {
 }
 
 int fa_version(void) { return kVersion; }
+
+int fa_row_kernel_register_check(int num_regs, int max_threads_per_block) {
+  t_last_error.clear();
+  return register_split_check(num_regs, max_threads_per_block);
+}
+
+void fa_test_override_kernel_registers(int num_regs) {
+  g_regs_override.store(num_regs > 0 ? num_regs : 0);
+}
 
 }  // extern "C"

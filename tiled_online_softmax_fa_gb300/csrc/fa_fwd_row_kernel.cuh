@@ -40,9 +40,16 @@ constexpr int kLoadWarpR = 13;
 // and were measured to cost ~500 cycles on the path S ready -> P ready.
 constexpr uint32_t kRowWarpsPerTile = 4;
 constexpr uint32_t kEpilogueWarps = 4;
+// Registers per thread the kernel must be compiled to (512 threads x 128 = the SM's 64K),
+// and the per-warpgroup shares setmaxnreg moves them to.  The shares add up to exactly
+// the launch's pool: a setmaxnreg.inc that asks for more than the pool can give waits
+// without a bound, so the host refuses to launch a build whose allocation differs from
+// kLaunchRegs (see the register check in the host code).
+constexpr int kLaunchRegs = 128;
 constexpr uint32_t kRegsSoftmax = 176, kRegsEpilogue = 72, kRegsControl = 88;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsEpilogue + 128 * kRegsControl <= kThreadsR * 128,
-              "register split exceeds the launch's registers");
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsEpilogue + 128 * kRegsControl ==
+                  kThreadsR * kLaunchRegs,
+              "the register split must hand out exactly the launch's registers");
 
 // Row statistics handed from a softmax thread to the epilogue thread of the same row.
 struct RowStats {
