@@ -88,10 +88,56 @@ def load_peaks():
 # --------------------------------------------------------------------------------------
 # clocks during the timed region
 # --------------------------------------------------------------------------------------
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the driver): the SM
+    clock, its maximum, the power draw and the active clock-event (throttle) reasons."""
+    CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        ok = False
+        try:   # the GPU torch calls `torch_index`, found by UUID (NVML ignores CUDA_VISIBLE_DEVICES)
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(torch_index).uuid)
+            ok = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) == 0
+        except Exception:  # noqa: BLE001 - an older torch without .uuid
+            ok = False
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(torch_index, ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle for the GPU")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.reasons_fn = fn
+        self.max_mhz = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.CLOCK_SM)
+
+    def _uint(self, fn, *args):
+        v = self.ct.c_uint()
+        if fn(self.dev, *args, self.ct.byref(v)) != 0:
+            return None
+        return int(v.value)
+
+    def sample(self) -> dict:
+        r = self.ct.c_ulonglong()
+        reasons = int(r.value) if self.reasons_fn(self.dev, self.ct.byref(r)) == 0 else 0
+        mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
+        return {"sm": self._uint(self.lib.nvmlDeviceGetClockInfo, self.CLOCK_SM), "max": self.max_mhz,
+                "power": mw / 1000.0 if mw is not None else None,
+                "reasons": [name for bit, name in self.REASONS.items() if reasons & bit]}
+
+
 class ClockSampler:
+    """Clocks and throttle reasons while the timed region runs.  NVML is polled in-process
+    every few milliseconds, so even a region of a few tens of milliseconds holds samples;
+    where NVML cannot be loaded, nvidia-smi is polled every 20 ms instead."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.004
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -99,18 +145,36 @@ class ClockSampler:
         self.proc = None
         self.thread = None
         self.active = False
+        self.stopped = False
+        self.source = None
 
     def start(self):
         try:
+            nvml = _Nvml(self.gpu)
+            self.source = f"NVML every {self.PERIOD_S * 1e3:.0f} ms"
+            self.thread = threading.Thread(target=self._poll, args=(nvml,), daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            pass
+        try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "200"],
+                 "-i", str(self.gpu), "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
+        self.source = "nvidia-smi every 20 ms"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+
+    def _poll(self, nvml):
+        while not self.stopped:
+            rec = nvml.sample()
+            rec["in_region"] = self.active
+            self.samples.append(rec)
+            time.sleep(self.PERIOD_S)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -120,14 +184,16 @@ class ClockSampler:
             try:
                 rec = {"sm": float(parts[1]), "max": float(parts[2]),
                        "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
-                       "hw_slowdown": parts[5], "hw_thermal": parts[6],
-                       "sw_thermal": parts[7], "sw_power_cap": parts[8]}
+                       "reasons": [name for key, name in ((5, "hw_slowdown"), (6, "hw_thermal_slowdown"),
+                                                          (7, "sw_thermal_slowdown"), (8, "sw_power_cap"))
+                                   if parts[key].lower() == "active"]}
             except ValueError:
                 continue
             rec["in_region"] = self.active
             self.samples.append(rec)
 
     def stop(self):
+        self.stopped = True
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -138,21 +204,16 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self):
-        region = [s for s in self.samples if s["in_region"]]
+        region = [s for s in self.samples if s["in_region"] and s["sm"] is not None]
         if not region:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        reasons = set()
-        for s in region:
-            for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
-                              ("sw_thermal", "sw_thermal_slowdown"),
-                              ("sw_power_cap", "sw_power_cap")):
-                if s[key].lower() == "active":
-                    reasons.add(name)
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({r for s in region for r in s["reasons"]})
         powers = [s["power"] for s in region if s["power"] is not None]
         return {"sm_mhz": statistics.median(s["sm"] for s in region),
-                "sm_max_mhz": max(s["max"] for s in region),
-                "reasons": sorted(reasons), "samples": len(region),
-                "power_w_max": max(powers) if powers else None}
+                "sm_max_mhz": max(s["max"] or 0 for s in region) or None,
+                "reasons": reasons, "samples": len(region),
+                "power_w_max": max(powers) if powers else None, "source": self.source}
 
 
 # --------------------------------------------------------------------------------------
@@ -449,9 +510,10 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         barrier(world)
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        h2d_bytes = 3 * q.numel() * 2
+        d2h_bytes = o.numel() * 2 + lse.numel() * 4
         e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": 3 * q.numel() * 2,
-               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                "steps": n_e2e, "ms_per_step": ms_e2e, "chunks_per_step": chunks,
                "launches_per_step": chunks}
         if fa.get_device_status(stream) != fa.FA_OK:
@@ -460,6 +522,37 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         if not (torch.equal(ho, o.cpu()) and torch.equal(hl, lse.cpu())):
             raise SystemExit("e2e outputs differ from the device outputs")
+        # The host link on this machine, measured here with the step's own buffers: the
+        # inputs copied in alone, the outputs copied out alone, and both at once.  The
+        # step cannot beat moving its inputs in and its outputs out, so that time (with
+        # both directions running at once) bounds the e2e rate.
+        def timed_copies(h2d: bool, d2h: bool, reps: int = 3) -> float:
+            best = float("inf")
+            for _ in range(reps):
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(s_in)
+                s_out.wait_event(t0)
+                if h2d:
+                    with torch.cuda.stream(s_in):
+                        for dst, src in ((qd, hq), (kd, hk), (vd, hv)):
+                            dst.copy_(src, non_blocking=True)
+                if d2h:
+                    with torch.cuda.stream(s_out):
+                        ho.copy_(o, non_blocking=True)
+                        hl.copy_(lse, non_blocking=True)
+                s_in.wait_stream(s_out)
+                t1.record(s_in)
+                torch.cuda.synchronize(dev)
+                best = min(best, t0.elapsed_time(t1))
+            return best
+        ms_in, ms_out, ms_both = timed_copies(True, False), timed_copies(False, True), \
+            timed_copies(True, True)
+        e2e.update(link_h2d_gbs=h2d_bytes / (ms_in * 1e-3) / 1e9,
+                   link_d2h_gbs=d2h_bytes / (ms_out * 1e-3) / 1e9,
+                   link_both_ms=ms_both,
+                   frac_of_link_bound=ms_both / ms_e2e,
+                   link_note="copies of the step's own pinned buffers, best of 3; "
+                             "frac_of_link_bound = (inputs in + outputs out, both at once) / e2e step")
 
     if sampler:
         sampler.stop()
