@@ -483,6 +483,25 @@ int grid_for(const DeviceState& dev, const fa_fwd_options* opts, int items) {
   return grid > items ? items : grid;
 }
 
+// The merge of a split launch: one warp per query row; the partial outputs of up to
+// 2 or 8 pieces are loaded up front (the smallest bucket that holds `splits`).
+template <int HD, int UNIT_ROWS>
+int launch_merge(const fa_sm103::Params& p, int64_t BH, int64_t N, cudaStream_t stream) {
+  const int64_t warps = BH * N;
+  const unsigned blocks = static_cast<unsigned>((warps + fa_sm103::kMergeThreads / 32 - 1) /
+                                                (fa_sm103::kMergeThreads / 32));
+  constexpr int T = fa_sm103::kMergeThreads;
+  if (p.splits <= 2)
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 2><<<blocks, T, 0, stream>>>(p);
+  else if (p.splits <= 8)
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 8><<<blocks, T, 0, stream>>>(p);
+  else
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 0><<<blocks, T, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
+  return FA_OK;
+}
+
 // ---- register split of the two-tile kernel ------------------------------------------
 // fa_fwd_row_kernel moves registers between its warpgroups with setmaxnreg (softmax up,
 // epilogue and control down); the shares add up to exactly the registers the block is
@@ -534,10 +553,12 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
   if (!smem_set) {
     cudaError_t e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         fa_sm103::rowk::row_kernel_smem<HD, false>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               fa_sm103::rowk::row_kernel_smem<HD, true>());
     if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
     smem_set = true;
   }
@@ -552,19 +573,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   set_schedule(p, grid, pick_order(opts, FA_KERNEL_TWO_TILE, BH, N, HD, causal, grid, splits));
   constexpr int kThr = fa_sm103::rowk::kThreadsR;
   if (splits > 1)
-    fa_sm103::rowk::fa_fwd_row_kernel<HD, true><<<grid, kThr, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    fa_sm103::rowk::fa_fwd_row_kernel<HD, true>
+        <<<grid, kThr, fa_sm103::rowk::row_kernel_smem<HD, true>(), stream>>>(mq, mk, mv, p);
   else
-    fa_sm103::rowk::fa_fwd_row_kernel<HD, false><<<grid, kThr, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    fa_sm103::rowk::fa_fwd_row_kernel<HD, false>
+        <<<grid, kThr, fa_sm103::rowk::row_kernel_smem<HD, false>(), stream>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
-  if (splits > 1) {
-    const int64_t warps = BH * N;
-    const int64_t blocks = (warps + fa_sm103::kMergeThreads / 32 - 1) / (fa_sm103::kMergeThreads / 32);
-    fa_sm103::fa_merge_kernel<HD, fa_sm103::kUnitRows><<<static_cast<unsigned>(blocks),
-                                                         fa_sm103::kMergeThreads, 0, stream>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
-  }
+  if (splits > 1) return launch_merge<HD, fa_sm103::kUnitRows>(p, BH, N, stream);
   return FA_OK;
 }
 
@@ -607,14 +623,7 @@ int launch_one(const void* q, const void* k, const void* v, void* o, float* lse,
     fa_sm103::one::fa_fwd_1tile_kernel<HD, false><<<grid, kThr, SMEM, stream>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
-  if (splits > 1) {
-    const int64_t warps = BH * N;
-    const int64_t blocks = (warps + fa_sm103::kMergeThreads / 32 - 1) / (fa_sm103::kMergeThreads / 32);
-    fa_sm103::fa_merge_kernel<HD, fa_sm103::one::kUnitRows1>
-        <<<static_cast<unsigned>(blocks), fa_sm103::kMergeThreads, 0, stream>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
-  }
+  if (splits > 1) return launch_merge<HD, fa_sm103::one::kUnitRows1>(p, BH, N, stream);
   return FA_OK;
 }
 

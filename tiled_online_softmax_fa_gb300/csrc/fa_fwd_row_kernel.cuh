@@ -39,6 +39,9 @@ constexpr int kLoadWarpR = 13;
 // after __syncwarp): 128 per-thread arrivals on one shared-memory word are serialised
 // and were measured to cost ~500 cycles on the path S ready -> P ready.
 constexpr uint32_t kRowWarpsPerTile = 4;
+// Dynamic shared memory of a launch: split launches add the epilogue's store blocks.
+template <int HD, bool SPLIT>
+constexpr int row_kernel_smem() { return Cfg<HD>::SMEM_BYTES + (SPLIT ? 4 * 4096 : 0); }
 constexpr uint32_t kEpilogueWarps = 4;
 // Registers per thread the kernel must be compiled to (512 threads x 128 = the SM's 64K),
 // and the per-warpgroup shares setmaxnreg moves them to.  The shares add up to exactly
@@ -211,16 +214,61 @@ fail:
 }
 
 // ------------------------------------------------------------------------------------
+// Coalesced stores of a split item's fp32 partial output.  Each lane holds one row, so
+// a direct store would touch 32 rows with 16 bytes each; instead a warp passes the rows
+// through a 4 KB shared-memory block of its own and writes whole 128-byte row pieces.
+// ------------------------------------------------------------------------------------
+constexpr int kEpiScratchBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
+
+// A warp's 32-row block (one row per lane) of RB bytes per row in its scratch: lane l
+// puts 16-byte piece c of row l with stage_piece (pieces rotated by row, piece_rot, so
+// the 8 lanes of a shared-memory phase hit the 8 16-byte bank groups of a 128-byte line
+// once each), then flush_rows reads the block back
+// with consecutive lanes on consecutive pieces of one row and writes whole rows: one
+// warp store covers 32*16/RB rows of RB contiguous bytes.  Rows >= rows_valid are not
+// written; gbase = first row's first byte, stride = bytes between rows in global memory.
+template <int RB>
+__device__ __forceinline__ int piece_rot(int r) {  // rows sharing a 128-byte line rotate alike
+  return (r / (128 / RB)) % (RB / 16);
+}
+
+template <int RB>
+__device__ __forceinline__ void stage_piece(uint32_t scratch, int lane, int c, uint32_t a,
+                                            uint32_t b, uint32_t cc, uint32_t d) {
+  st_shared_v4(scratch + lane * RB + ((c ^ piece_rot<RB>(lane)) * 16), a, b, cc, d);
+}
+
+template <int RB>
+__device__ __forceinline__ void flush_rows(uint32_t scratch, int lane, uint8_t* gbase, size_t stride,
+                                           int rows_valid) {
+  constexpr int P = RB / 16;   // 16-byte pieces per row
+  constexpr int RPI = 32 / P;  // rows one warp store covers
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int rr = i * RPI + lane / P, c = lane % P;
+    uint4 x;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                 : "r"(scratch + rr * RB + ((c ^ piece_rot<RB>(rr)) * 16)));
+    if (rr < rows_valid) *reinterpret_cast<uint4*>(gbase + rr * stride + c * 16) = x;
+  }
+  __syncwarp();  // the block is reused by the warp's next chunk
+}
+
+// ------------------------------------------------------------------------------------
 // epilogue (warpgroup 2): thread = one row of the Q tile being finished.  O = acc /
 // l_round rounded to bf16 (or, for a split item, the normalised fp32 partial O), and
 // lse = (m_ref + log2 l_exact) ln 2.
 // ------------------------------------------------------------------------------------
 template <int HD, bool SPLIT>
-__device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Params& p) {
+__device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Params& p,
+                              uint8_t* sScratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
   const int lrow = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t scratch = smem_u32(sScratch) + wq * kEpiScratchBytes;  // split items only
   uint32_t cnt[2] = {0, 0};  // units finished per Q tile
   for (int k = 0; k < p.num_rounds; ++k) {
     const int u = item_of(k, p);
@@ -245,22 +293,30 @@ __device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Pa
       const float inv_l = 1.f / l_round;
       constexpr int NV = HD < 32 ? HD : 32;  // columns of O per 32-column TMEM load
       if constexpr (SPLIT) {
-        const size_t slot = static_cast<size_t>(u) * kUnitRows + t * kBlockM + lrow;
-        float* orow = p.ws_o + slot * HD;
+        // normalised fp32 partial O: chunks of 32 columns (128 bytes per row), read from
+        // TMEM 16 columns at a time
+        constexpr int CW = HD < 32 ? HD : 32;
+        const int row0w = it.row0 + t * kBlockM + wq * 32;  // the warp's first row
+        const size_t slot0 = static_cast<size_t>(u) * kUnitRows + t * kBlockM + wq * 32;
+        uint8_t* gbase = reinterpret_cast<uint8_t*>(p.ws_o + slot0 * HD);
+#pragma unroll 1
+        for (int c0 = 0; c0 < HD; c0 += CW) {
 #pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(tO + c0, o);
-          tmem_wait_ld(o);
-          if (store) {
+          for (int h = 0; h < CW; h += 16) {
+            uint32_t o[16];
+            tmem_ld_x16(tO + c0 + h, o);
+            tmem_wait_ld(o);
 #pragma unroll
-            for (int v4 = 0; v4 < NV; v4 += 4)
-              *reinterpret_cast<float4*>(orow + c0 + v4) =
-                  make_float4(__uint_as_float(o[v4]) * inv_l, __uint_as_float(o[v4 + 1]) * inv_l,
-                              __uint_as_float(o[v4 + 2]) * inv_l, __uint_as_float(o[v4 + 3]) * inv_l);
+            for (int q = 0; q < 4; ++q)
+              stage_piece<CW * 4>(scratch, lane, h / 4 + q,
+                                  __float_as_uint(__uint_as_float(o[4 * q + 0]) * inv_l),
+                                  __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv_l),
+                                  __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv_l),
+                                  __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv_l));
           }
+          flush_rows<CW * 4>(scratch, lane, gbase + c0 * 4, static_cast<size_t>(HD) * 4, p.N - row0w);
         }
-        if (store) p.ws_lse[slot] = (m_ref + lg2_approx(l_exact)) * kLn2;
+        if (store) p.ws_lse[slot0 + lane] = (m_ref + lg2_approx(l_exact)) * kLn2;
       } else {
         __nv_bfloat16* orow = p.o + (static_cast<size_t>(it.bh) * p.N + row) * HD;
 #pragma unroll
@@ -304,6 +360,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + C::SMEM_Q;
+  uint8_t* sScratch = sRing + C::NSLOT * C::TILE_BYTES;  // split launches: epilogue store blocks
   __shared__ Barriers b;
   __shared__ RowStats rs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -342,7 +399,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
     setmaxnreg_dec<128>();
   } else if (warp < kMmaWarpR) {
     setmaxnreg_dec<kRegsEpilogue>();
-    epilogue_role<HD, SPLIT>(tmem, b, rs, p);
+    epilogue_role<HD, SPLIT>(tmem, b, rs, p, sScratch);
     setmaxnreg_inc<128>();
   } else {
     setmaxnreg_dec<kRegsControl>();

@@ -35,20 +35,21 @@ __device__ __forceinline__ void load_partial(const float* src, float (&x)[E]) {
   }
 }
 
-constexpr int kMergeEager = 8;  // up to this many pieces, partial outputs load up front
-
 // One warp per query row.  The row's pieces are found in the lanes (lane s holds piece s
 // and s + 32): their lse values give the row maximum and the weights exp(lse_s - m)
 // through two warp reductions.  Each lane reads its E columns of every piece and writes
-// its E bf16 outputs with one vector store.  With at most kMergeEager pieces the
-// partial outputs are loaded before the lse values are known, so a row costs one memory
-// round trip instead of two; a piece without an admissible key for the row (its key
-// range starts past the row's diagonal tile, its partial never written) has weight 0
-// and its loaded values are not used.
+// its E bf16 outputs with one vector store.  With at most NP pieces (NP = 2 or 8; the
+// host picks the smallest that holds the launch's split count) the partial outputs are
+// loaded before the lse values are known, so a row costs one memory round trip instead
+// of two, and the registers for them are sized to NP, so launches of few pieces keep
+// more rows in flight per SM (memory-bound: bytes in flight set the rate); NP = 0 loads
+// each piece once its weight is known.  A piece without an admissible key for the row
+// (its key range starts past the row's diagonal tile, its partial never written) has
+// weight 0 and its loaded values are not used.
 // UNIT_ROWS: the query rows of the split kernel's work unit -- kUnitRows (two-tile
 // kernel: a piece may hold no admissible key for tile 0's rows) or kUnitRows1 (one-tile
 // kernel: every non-empty piece holds some).
-template <int HD, int UNIT_ROWS>
+template <int HD, int UNIT_ROWS, int NP>
 __global__ void __launch_bounds__(kMergeThreads)
     fa_merge_kernel(const Params p) {
   static_assert(HD <= 256, "head dims 16 to 256");
@@ -65,11 +66,11 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int u = g * p.group_heads * p.nqb + (p.nqb - 1 - qb) * heads + (bh - first);
   const size_t base = static_cast<size_t>(u) * p.splits;
   const bool active = lane < kLanes;
-  const bool eager = p.splits <= kMergeEager;
-  float xe[kMergeEager][E];
+  constexpr bool eager = NP > 0;
+  float xe[eager ? NP : 1][E];
   if (eager && active) {
 #pragma unroll
-    for (int sp = 0; sp < kMergeEager; ++sp)
+    for (int sp = 0; sp < (eager ? NP : 1); ++sp)
       if (sp < p.splits)
         load_partial<E>(p.ws_o + ((base + sp) * UNIT_ROWS + rin) * HD + lane * E, xe[sp]);
   }
@@ -106,9 +107,9 @@ __global__ void __launch_bounds__(kMergeThreads)
   float acc[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) acc[i] = 0.f;
-  if (eager) {
+  if constexpr (eager) {
 #pragma unroll
-    for (int sp = 0; sp < kMergeEager; ++sp) {
+    for (int sp = 0; sp < NP; ++sp) {
       if (sp >= p.splits) break;
       const float wgt = __shfl_sync(0xFFFFFFFFu, w[0], sp);
       if (wgt != 0.f && active) {
