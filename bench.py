@@ -324,6 +324,8 @@ def parse_args(argv=None):
     ap.add_argument("--order", choices=["auto", "one", "group", "shifted"], default="auto",
                     help="sweep: pin the unit order (one snake / a snake per head group, odd "
                     "groups mirrored / shifted past the previous group's last round)")
+    ap.add_argument("--block-kv", type=int, default=0, help="sweep: keys per K/V tile (0 = the "
+                    "library's choice, 64 or 128)")
     ap.add_argument("--sweep-shapes", default="", help="sweep: 'B,H,N;B,H,N;...' (overrides "
                     "--B, --H and --sweep-n)")
     ap.add_argument("--sweep-launches", type=int, default=20, help="timed launches per length "
@@ -635,8 +637,8 @@ def run_sweep(args):
                 kernel = fa.FA_KERNEL_ONE_TILE if d == 256 else fa.FA_KERNEL_TWO_TILE
         order = {"auto": fa.FA_ORDER_AUTO, "one": fa.FA_ORDER_ONE_SNAKE,
                  "group": fa.FA_ORDER_GROUP_SNAKES, "shifted": fa.FA_ORDER_SHIFTED_SNAKES}[args.order]
-        opts = fa.FwdOptions(kernel=kernel, order=order) if (splits == 1 or args.kernel != "auto") \
-            else None
+        opts = fa.FwdOptions(kernel=kernel, order=order, block_kv=args.block_kv) \
+            if (splits == 1 or args.kernel != "auto" or args.block_kv) else None
         if args.materialised:
             splits = 1
             ws = torch.empty(fa.materialised_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
@@ -664,6 +666,7 @@ def run_sweep(args):
             shown = fa.fwd_plan(B, H, N, d, causal, allow_split=args.splits == 0,
                                 with_order=True)[2]
         rec = {"N": N, "B": B, "H": H, "d": d, "causal": causal, "splits": splits,
+               "block_kv": args.block_kv or 128,
                "order": {fa.FA_ORDER_ONE_SNAKE: "one snake", fa.FA_ORDER_GROUP_SNAKES: "group snakes",
                          fa.FA_ORDER_SHIFTED_SNAKES: "shifted snakes", None: None}[shown],
                "kernel": None if args.materialised else

@@ -93,6 +93,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   order               FA_ORDER_AUTO (0): the library's choice; FA_ORDER_ONE_SNAKE or
  *                       FA_ORDER_GROUP_SNAKES pins how work units are handed to the
  *                       CTAs (see fa_order).  Results are identical either way.
+ *   block_kv            keys per K/V tile, the pages' `block_kv` (aiml.sh "Speed up long
+ *                       contexts with FlashAttention", lab.py `tiled_flash_attention`):
+ *                       0 = automatic (128), 128, or 64.  64 runs the two-tile kernel
+ *                       (head dims 16-128; FA_ERR_UNSUPPORTED at 256 or with the one-tile
+ *                       kernel pinned) with 64-key score tiles: half the keys per online-
+ *                       softmax step and per MMA pair.  Any other value: FA_ERR_INVALID_ARG.
+ *                       With 64 and splits = 0 the split count is the heuristic's
+ *                       (fa_splitkv_auto_splits).
+ * Zero-initialise the whole struct: fields are appended as the library grows (version
+ * 0.3.0 appended block_kv).
  */
 typedef struct {
     int64_t wait_budget_cycles;
@@ -100,6 +110,7 @@ typedef struct {
     int32_t max_ctas;
     int32_t kernel;
     int32_t order;
+    int32_t block_kv;
 } fa_fwd_options;
 
 /*

@@ -34,11 +34,13 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
 
 
 def run_gpu(q, k, v, causal: bool, scale: float, want_lse: bool = True,
-            kernel: int = fa.FA_KERNEL_AUTO):
-    """fa_fwd on cuda:0; `kernel` pins FA_KERNEL_TWO_TILE or FA_KERNEL_ONE_TILE."""
+            kernel: int = fa.FA_KERNEL_AUTO, block_kv: int = 0):
+    """fa_fwd on cuda:0; `kernel` pins FA_KERNEL_TWO_TILE or FA_KERNEL_ONE_TILE, `block_kv`
+    the keys per K/V tile (0 = the library's choice)."""
     dev = torch.device("cuda:0")
     qd, kd, vd = (t.to(dev) for t in (q, k, v))
-    opts = fa.FwdOptions(kernel=kernel) if kernel != fa.FA_KERNEL_AUTO else None
+    opts = (fa.FwdOptions(kernel=kernel, block_kv=block_kv)
+            if kernel != fa.FA_KERNEL_AUTO or block_kv else None)
     o, lse = fa.fa_fwd(qd, kd, vd, causal=causal, scale=scale, want_lse=want_lse, options=opts)
     status = fa.get_device_status()
     assert status == fa.FA_OK, fa.strerror(status)
@@ -86,14 +88,14 @@ def compare(og: np.ndarray, lg, o64: np.ndarray, lse64: np.ndarray) -> dict:
 
 def check_case(w: workloads.Workload, causal: bool, B=None, H=None, N=None, d=None, seed=None,
                rows: np.ndarray | None = None, scale: float | None = None,
-               kernel: int = fa.FA_KERNEL_AUTO):
+               kernel: int = fa.FA_KERNEL_AUTO, block_kv: int = 0):
     q, k, v = workloads.make_inputs(w, B=B, H=H, N=N, d=d, seed=seed)
     Bv, Hv, Nv, dv = q.shape
     if scale is None:
         scale = float(np.float32(1.0 / np.sqrt(dv)))
     if rows is None:
         rows = workloads.select_rows(w, B=Bv, H=Hv, N=Nv, seed=seed)
-    o, lse = run_gpu(q, k, v, causal, scale, kernel=kernel)
+    o, lse = run_gpu(q, k, v, causal, scale, kernel=kernel, block_kv=block_kv)
     og, lg = gather_rows(o, lse, rows)
     o64, lse64 = oracle.attn_rows(q, k, v, rows, causal, scale)
     return compare(og, lg, o64, lse64), (q, k, v, o, lse)

@@ -27,7 +27,7 @@ def test_every_header_belongs_to_a_library():
 def test_library_builds_and_loads():
     lib = fa.load_library()
     assert isinstance(lib, ctypes.CDLL)
-    assert fa.version() == 200
+    assert fa.version() == 300
 
 
 def test_every_declared_symbol_is_exported():
@@ -232,3 +232,17 @@ def test_noalloc_range_checks_come_before_any_size_arithmetic(B, H, N, splits):
                                        True, 0.088, splits)
     assert rc == fa.FA_ERR_UNSUPPORTED
     assert fa.last_error() != ""
+
+
+@pytest.mark.parametrize("block_kv,d,kernel,want", [
+    (32, 128, 0, fa.FA_ERR_INVALID_ARG),       # neither 64 nor 128
+    (256, 64, 0, fa.FA_ERR_INVALID_ARG),
+    (-64, 64, 0, fa.FA_ERR_INVALID_ARG),
+    (64, 256, 0, fa.FA_ERR_UNSUPPORTED),       # 64-key tiles: the two-tile kernel only
+    (64, 128, fa.FA_KERNEL_ONE_TILE, fa.FA_ERR_UNSUPPORTED),
+])
+def test_block_kv_errors(block_kv, d, kernel, want):
+    # rejected before any CUDA call
+    assert _call(d=d, options=fa.FwdOptions(block_kv=block_kv, kernel=kernel)) == want
+    assert fa.last_error() != ""
+

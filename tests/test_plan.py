@@ -199,8 +199,10 @@ def _call_opts(d, **opt):
 
 
 def test_options_struct_layout():
-    assert ctypes.sizeof(fa.FwdOptions) == 24
+    # the C struct: int64 budget, then five int32 fields (block_kv appended last, 0.3.0)
+    assert ctypes.sizeof(fa.FwdOptions) == 32
     assert fa.FwdOptions.kernel.offset == 16 and fa.FwdOptions.order.offset == 20
+    assert fa.FwdOptions.block_kv.offset == 24
 
 
 @pytest.mark.parametrize("d,opt,want", [

@@ -47,7 +47,8 @@ class FwdOptions(ctypes.Structure):
                 ("inject_skip_kv_load", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32),
                 ("kernel", ctypes.c_int32),
-                ("order", ctypes.c_int32)]
+                ("order", ctypes.c_int32),
+                ("block_kv", ctypes.c_int32)]
 
 
 class FAError(RuntimeError):

@@ -26,7 +26,7 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 namespace {
 
-constexpr int kVersion = 200;  // 0.2.0 (fa_fwd_options gained `kernel`)
+constexpr int kVersion = 300;  // 0.3.0 (fa_fwd_options gained `block_kv`)
 constexpr int kMaxDevices = 64;
 constexpr long long kDefaultBudget = 2000000000LL;  // ~1 s of SM clock
 
@@ -51,7 +51,7 @@ struct DeviceState {
   bool probed = false;
   bool arch_ok = false;
   int num_sms = 0;
-  bool smem_set[5] = {false, false, false, false, false};      // two-tile kernel, per head dim
+  bool smem_set[5][2] = {};                                    // two-tile kernel, per head dim and key tile
   bool smem_set_one[5] = {false, false, false, false, false};  // one-tile kernel
 };
 
@@ -75,14 +75,16 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// Encode a [BH, N, d] bf16 tensor as a 3-D tiled map with a (W x 128 x 1) box.
-int encode_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t d) {
+// Encode a [BH, N, d] bf16 tensor as a 3-D tiled map with a (W x rows x 1) box: 128 rows
+// for Q tiles, the key-tile width for K and V.
+int encode_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t d,
+               int rows = fa_sm103::kBlockM) {
   const int w = d < 64 ? static_cast<int>(d) : 64;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2),
                                  static_cast<cuuint64_t>(N * d * 2)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(w), fa_sm103::kBlockM, 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(w), static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = w * 2 == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : w * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -485,18 +487,18 @@ int grid_for(const DeviceState& dev, const fa_fwd_options* opts, int items) {
 
 // The merge of a split launch: one warp per query row; the partial outputs of up to
 // 2 or 8 pieces are loaded up front (the smallest bucket that holds `splits`).
-template <int HD, int UNIT_ROWS>
+template <int HD, int UNIT_ROWS, int BN = fa_sm103::kBlockN>
 int launch_merge(const fa_sm103::Params& p, int64_t BH, int64_t N, cudaStream_t stream) {
   const int64_t warps = BH * N;
   const unsigned blocks = static_cast<unsigned>((warps + fa_sm103::kMergeThreads / 32 - 1) /
                                                 (fa_sm103::kMergeThreads / 32));
   constexpr int T = fa_sm103::kMergeThreads;
   if (p.splits <= 2)
-    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 2><<<blocks, T, 0, stream>>>(p);
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 2, BN><<<blocks, T, 0, stream>>>(p);
   else if (p.splits <= 8)
-    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 8><<<blocks, T, 0, stream>>>(p);
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 8, BN><<<blocks, T, 0, stream>>>(p);
   else
-    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 0><<<blocks, T, 0, stream>>>(p);
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 0, BN><<<blocks, T, 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
   return FA_OK;
@@ -523,10 +525,10 @@ int register_split_check(int num_regs, int max_threads) {
   return set_error(FA_ERR_UNSUPPORTED, buf);
 }
 
-template <int HD>
+template <int HD, int BN>
 int check_row_kernel_registers() {
-  const void* fns[2] = {reinterpret_cast<const void*>(fa_sm103::rowk::fa_fwd_row_kernel<HD, false>),
-                        reinterpret_cast<const void*>(fa_sm103::rowk::fa_fwd_row_kernel<HD, true>)};
+  const void* fns[2] = {reinterpret_cast<const void*>(fa_sm103::rowk::fa_fwd_row_kernel<HD, BN, false>),
+                        reinterpret_cast<const void*>(fa_sm103::rowk::fa_fwd_row_kernel<HD, BN, true>)};
   for (const void* fn : fns) {
     cudaFuncAttributes a;
     const cudaError_t e = cudaFuncGetAttributes(&a, fn);
@@ -538,31 +540,33 @@ int check_row_kernel_registers() {
   return FA_OK;
 }
 
-template <int HD>
+// The two-tile kernel (256-row units) with key tiles of BN keys (128, or 64 on request).
+template <int HD, int BN>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
            int64_t N, int causal, float scale, cudaStream_t stream, const DeviceState& dev,
            bool& smem_set, const fa_fwd_options* opts, int splits, void* workspace) {
-  using C = fa_sm103::Cfg<HD>;
   CUtensorMap mq, mk, mv;
   int st;
-  // the first launch per device and head dim (and every launch while the test hook is set)
-  if ((!smem_set || g_regs_override.load() > 0) && (st = check_row_kernel_registers<HD>()) != FA_OK)
+  // the first launch per device, head dim and key tile (and every launch while the test
+  // hook is set)
+  if ((!smem_set || g_regs_override.load() > 0) && (st = check_row_kernel_registers<HD, BN>()) != FA_OK)
     return st;
   if ((st = encode_map(&mq, q, BH, N, HD)) != FA_OK) return st;
-  if ((st = encode_map(&mk, k, BH, N, HD)) != FA_OK) return st;
-  if ((st = encode_map(&mv, v, BH, N, HD)) != FA_OK) return st;
+  if ((st = encode_map(&mk, k, BH, N, HD, BN)) != FA_OK) return st;
+  if ((st = encode_map(&mv, v, BH, N, HD, BN)) != FA_OK) return st;
   if (!smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, false>,
+    cudaError_t e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, BN, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         fa_sm103::rowk::row_kernel_smem<HD, false>());
+                                         fa_sm103::rowk::row_kernel_smem<HD, BN, false>());
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, true>,
+      e = cudaFuncSetAttribute(fa_sm103::rowk::fa_fwd_row_kernel<HD, BN, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               fa_sm103::rowk::row_kernel_smem<HD, true>());
+                               fa_sm103::rowk::row_kernel_smem<HD, BN, true>());
     if (e != cudaSuccess) return cuda_error("cudaFuncSetAttribute", e);
     smem_set = true;
   }
   fa_sm103::Params p = base_params(o, lse, BH, N, HD, fa_sm103::kUnitRows, causal, scale, opts);
+  p.nkv = static_cast<int>((N + BN - 1) / BN);
   p.splits = splits;
   p.num_items = p.num_units * splits;
   p.ws_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
@@ -573,14 +577,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   set_schedule(p, grid, pick_order(opts, FA_KERNEL_TWO_TILE, BH, N, HD, causal, grid, splits));
   constexpr int kThr = fa_sm103::rowk::kThreadsR;
   if (splits > 1)
-    fa_sm103::rowk::fa_fwd_row_kernel<HD, true>
-        <<<grid, kThr, fa_sm103::rowk::row_kernel_smem<HD, true>(), stream>>>(mq, mk, mv, p);
+    fa_sm103::rowk::fa_fwd_row_kernel<HD, BN, true>
+        <<<grid, kThr, fa_sm103::rowk::row_kernel_smem<HD, BN, true>(), stream>>>(mq, mk, mv, p);
   else
-    fa_sm103::rowk::fa_fwd_row_kernel<HD, false>
-        <<<grid, kThr, fa_sm103::rowk::row_kernel_smem<HD, false>(), stream>>>(mq, mk, mv, p);
+    fa_sm103::rowk::fa_fwd_row_kernel<HD, BN, false>
+        <<<grid, kThr, fa_sm103::rowk::row_kernel_smem<HD, BN, false>(), stream>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("kernel launch", e);
-  if (splits > 1) return launch_merge<HD, fa_sm103::kUnitRows>(p, BH, N, stream);
+  if (splits > 1) return launch_merge<HD, fa_sm103::kUnitRows, BN>(p, BH, N, stream);
   return FA_OK;
 }
 
@@ -720,6 +724,14 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
     return set_error(FA_ERR_INVALID_ARG, "negative option");
   if (opts && (opts->order < FA_ORDER_AUTO || opts->order > FA_ORDER_SHIFTED_SNAKES))
     return set_error(FA_ERR_INVALID_ARG, "unknown item order");
+  const int block_kv = (opts && opts->block_kv != 0) ? opts->block_kv : 128;
+  if (block_kv != 64 && block_kv != 128)
+    return set_error(FA_ERR_INVALID_ARG, "block_kv must be 0 (automatic), 64 or 128");
+  if (block_kv == 64) {  // 64-key tiles: the two-tile kernel only
+    if (d == 256 || kernel == FA_KERNEL_ONE_TILE)
+      return set_error(FA_ERR_UNSUPPORTED, "64-key tiles run on the two-tile kernel (head dims 16 to 128)");
+    kernel = FA_KERNEL_TWO_TILE;
+  }
   if (kernel < FA_KERNEL_AUTO || kernel > FA_KERNEL_ONE_TILE)
     return set_error(FA_ERR_INVALID_ARG, "unknown kernel");
   if (kernel == FA_KERNEL_TWO_TILE && d == 256)
@@ -742,7 +754,15 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   st = device_state(&dev);
   if (st != FA_OK) return st;
   if (!dev->arch_ok) return set_error(FA_ERR_ARCH, "device is not sm_103 (GB300-class)");
-  if (splits == 0) {
+  if (splits == 0 && block_kv == 64) {
+    // the two-tile kernel, split as the heuristic says (within the workspace given)
+    const int max_splits =
+        workspace ? splits_fitting(BH, N, d, static_cast<int64_t>(workspace_size)) : 1;
+    splits = std::min(choose_splits(BH, N, dev->num_sms, causal), max_splits);
+    if (splits > 1 && !workspace_fits(workspace, workspace_size, BH, N, d, splits, q, k, v, o,
+                                      bytes, lse, lse_bytes))
+      return FA_ERR_INVALID_ARG;
+  } else if (splits == 0) {
     // plan among the split counts the workspace can hold
     const int max_splits =
         workspace ? splits_fitting(BH, N, d, static_cast<int64_t>(workspace_size)) : 1;
@@ -771,12 +791,20 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
       default: return launch_one<256>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, set_one, opts, splits, workspace);
     }
   }
-  bool& smem_set = dev->smem_set[hd];
+  bool& smem_set = dev->smem_set[hd][block_kv == 64 ? 1 : 0];
+  if (block_kv == 64) {
+    switch (hd) {
+      case 0: return launch<16, 64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+      case 1: return launch<32, 64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+      case 2: return launch<64, 64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+      default: return launch<128, 64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    }
+  }
   switch (hd) {
-    case 0: return launch<16>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
-    case 1: return launch<32>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
-    case 2: return launch<64>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
-    default: return launch<128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    case 0: return launch<16, 128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    case 1: return launch<32, 128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    case 2: return launch<64, 128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
+    default: return launch<128, 128>(q, k, v, o, lse, BH, N, causal, scale, s, *dev, smem_set, opts, splits, workspace);
   }
 }
 

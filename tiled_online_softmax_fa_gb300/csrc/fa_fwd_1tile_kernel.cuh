@@ -163,6 +163,12 @@ __device__ __forceinline__ bool warp_wait1(uint64_t* bar, uint32_t parity, const
   const bool ok = wait1(bar, parity, p, b);
   return __all_sync(0xFFFFFFFFu, ok);
 }
+// The issuer's wait: warp-wide when the whole warp runs the issuer.
+template <bool WARP>
+__device__ __forceinline__ bool wait1w(uint64_t* bar, uint32_t parity, const Params& p, Barriers1& b) {
+  if constexpr (WARP) return warp_wait1(bar, parity, p, b);
+  return wait1(bar, parity, p, b);
+}
 
 // ------------------------------------------------------------------------------------
 // TMA producer (one lane).  Ring order per item of key tiles [k0, k1): K_k0, K_k0+1,
@@ -238,7 +244,8 @@ drain:
 // ------------------------------------------------------------------------------------
 // MMA issuer (one lane)
 // ------------------------------------------------------------------------------------
-template <int HD, bool SPLIT>
+// WARP: run by the whole warp (one elected lane issues) or by one thread (head dim 256).
+template <int HD, bool SPLIT, bool WARP>
 __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1& b,
                           const Params& p) {
   using C = Cfg<HD>;
@@ -255,46 +262,46 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
     const int n = k1 - k0;  // key tiles of this item; tile j of the loops is k0 + j
     const uint32_t qb = units % QB;
     const uint32_t q_addr = smem_u32(sQ + qb * C::TILE_BYTES);
-    if (!wait1(&b.q_full[qb], (units / QB) & 1, p, b)) goto fail;
+    if (!wait1w<WARP>(&b.q_full[qb], (units / QB) & 1, p, b)) goto fail;
     ++units;
     // S(0) and S(1) into the two S buffers
     for (int j = 0; j < 2 && j < n; ++j) {
       const uint32_t ks = ring % NS;
-      if (!wait1(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
+      if (!wait1w<WARP>(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
       ++ring;
       tc_fence_after_sync();
-      issue_s<HD>(tmem + (j == 0 ? kColS0_1 : kColS1_1), q_addr, ring_addr + ks * C::TILE_BYTES);
-      mma_commit(&b.s_full[j]);
-      mma_commit(&b.slot_empty[ks]);
+      issue_s<HD, kBlockN, WARP>(tmem + (j == 0 ? kColS0_1 : kColS1_1), q_addr, ring_addr + ks * C::TILE_BYTES);
+      mma_commit<WARP>(&b.s_full[j]);
+      mma_commit<WARP>(&b.slot_empty[ks]);
     }
-    if (n <= 2) mma_commit(&b.q_empty[qb]);  // every S MMA of the unit is issued
+    if (n <= 2) mma_commit<WARP>(&b.q_empty[qb]);  // every S MMA of the unit is issued
     for (int j = 0; j < n; ++j) {
       const int sb = j & 1;
       const uint32_t colS = sb == 0 ? kColS0_1 : kColS1_1;
       const uint32_t vs = ring % NS;
-      if (!wait1(&b.slot_full[vs], (ring / NS) & 1, p, b)) goto fail;
+      if (!wait1w<WARP>(&b.slot_full[vs], (ring / NS) & 1, p, b)) goto fail;
       ++ring;
       if (j == 0) {  // O must have been read out by the previous item's epilogue
-        if (!wait1(&b.o_empty, (oe_cnt & 1) ^ 1, p, b)) goto fail;
+        if (!wait1w<WARP>(&b.o_empty, (oe_cnt & 1) ^ 1, p, b)) goto fail;
         ++oe_cnt;
       }
       uint32_t& p_cnt = sb == 0 ? p_cnt0 : p_cnt1;
-      if (!wait1(&b.p_full[sb], p_cnt & 1, p, b)) goto fail;
+      if (!wait1w<WARP>(&b.p_full[sb], p_cnt & 1, p, b)) goto fail;
       ++p_cnt;
       tc_fence_after_sync();
-      issue_pv<HD>(tmem + kColO_1, tmem + colS, ring_addr + vs * C::TILE_BYTES, j > 0);
-      mma_commit(&b.pv_done);
-      if (j == n - 1) mma_commit(&b.o_full);
-      mma_commit(&b.slot_empty[vs]);
+      issue_pv<HD, kBlockN, WARP>(tmem + kColO_1, tmem + colS, ring_addr + vs * C::TILE_BYTES, j > 0);
+      mma_commit<WARP>(&b.pv_done);
+      if (j == n - 1) mma_commit<WARP>(&b.o_full);
+      mma_commit<WARP>(&b.slot_empty[vs]);
       if (j + 2 < n) {
         const uint32_t ks = ring % NS;
-        if (!wait1(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
+        if (!wait1w<WARP>(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
         ++ring;
         tc_fence_after_sync();
-        issue_s<HD>(tmem + colS, q_addr, ring_addr + ks * C::TILE_BYTES);
-        mma_commit(&b.s_full[sb]);
-        mma_commit(&b.slot_empty[ks]);
-        if (j + 2 == n - 1) mma_commit(&b.q_empty[qb]);
+        issue_s<HD, kBlockN, WARP>(tmem + colS, q_addr, ring_addr + ks * C::TILE_BYTES);
+        mma_commit<WARP>(&b.s_full[sb]);
+        mma_commit<WARP>(&b.slot_empty[ks]);
+        if (j + 2 == n - 1) mma_commit<WARP>(&b.q_empty[qb]);
       }
     }
   }
@@ -302,7 +309,7 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
 fail:
   raise_abort1(b);
 drain:
-  mma_commit(&b.drain);
+  mma_commit<WARP>(&b.drain);
   drain_bar(&b.drain, 0, p);
 }
 
@@ -504,7 +511,10 @@ __global__ void __launch_bounds__(kThreads1, 1)
   if (warp < kSoftmaxWarps1) {
     softmax_role1<HD, SPLIT>(tmem, b, xchg, p);
   } else if (warp == kMmaWarp1) {
-    if (lane == 0) mma_role1<HD, SPLIT>(sQ, sRing, tmem, b, p);
+    if constexpr (HD != 256)
+      mma_role1<HD, SPLIT, true>(sQ, sRing, tmem, b, p);  // the whole warp; one elected lane issues
+    else if (lane == 0)
+      mma_role1<HD, SPLIT, false>(sQ, sRing, tmem, b, p);
     __syncwarp();
   } else if (warp == kLoadWarp1) {
     if (lane == 0) load_role1<HD, SPLIT>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);

@@ -45,26 +45,34 @@ namespace fa_sm103 {
 __device__ unsigned int g_device_status;
 
 constexpr int kBlockM = 128;                // query rows per Q tile (TMEM lanes)
-constexpr int kBlockN = 128;                // keys per K/V tile
+constexpr int kBlockN = 128;                // keys per K/V tile (the two-tile kernel also runs 64)
 constexpr int kUnitRows = 2 * kBlockM;      // query rows per work unit
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 constexpr float kRescaleLog2 = 8.0f;        // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.693147180559945309f;
 
-template <int HD>
+// Tile shapes for head dim HD and key tiles of BN keys (BN = 128, or 64 on the two-tile
+// kernel).  Q tiles are always 128 rows; K and V tiles are BN rows.
+template <int HD, int BN = kBlockN>
 struct Cfg {
   static_assert(HD == 16 || HD == 32 || HD == 64 || HD == 128 || HD == 256, "head dim");
+  static_assert(BN == 64 || BN == 128, "key tile width");
   static constexpr int W = HD < 64 ? HD : 64;          // elements per swizzled smem row
   static constexpr int SWB = 2 * W;                     // bytes per swizzled smem row
   static constexpr int NCH = HD / W;                    // row chunks across the head dim
-  static constexpr int TILE_BYTES = kBlockM * HD * 2;   // one 128-row bf16 tile
-  static constexpr int CHUNK_BYTES = kBlockM * SWB;     // one chunk of a tile
-  static constexpr int NSLOT = HD == 128 ? 4 : 8;       // K/V ring depth
+  static constexpr int TILE_BYTES = kBlockM * HD * 2;   // one 128-row bf16 tile (Q)
+  static constexpr int CHUNK_BYTES = kBlockM * SWB;     // one chunk of a Q tile
+  static constexpr int KV_TILE_BYTES = BN * HD * 2;     // one K or V tile
+  static constexpr int KV_CHUNK_BYTES = BN * SWB;       // one chunk of a K or V tile
+  // K/V ring: 4 x 32 KB at HD = 128 and BN = 128, otherwise as many tiles as fit 128 KB
+  // (at most 8)
+  static constexpr int NSLOT = (HD == 128 && BN == 128) ? 4
+                               : ((128 * 1024) / KV_TILE_BYTES < 8 ? (128 * 1024) / KV_TILE_BYTES : 8);
   static constexpr int SMEM_Q = 2 * TILE_BYTES;
-  static constexpr int SMEM_BYTES = SMEM_Q + NSLOT * TILE_BYTES + 1024;  // + alignment pad
+  static constexpr int SMEM_BYTES = SMEM_Q + NSLOT * KV_TILE_BYTES + 1024;  // + alignment pad
   static constexpr uint32_t SWZ = swizzle_code(SWB);
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(kBlockM, kBlockN, false);
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(kBlockM, BN, false);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(kBlockM, HD, true);
 };
 
@@ -73,7 +81,7 @@ struct Params {
   float* lse;         // [BH, N] or null
   int BH;             // batch * heads
   int N;              // sequence length
-  int nkv;            // ceil(N / 128)
+  int nkv;            // ceil(N / key tile width)
   int nqb;            // ceil(N / 256)
   int num_units;      // nqb * BH
   int splits;         // KV ranges per unit (1 = no split)
@@ -148,11 +156,13 @@ __device__ __forceinline__ int item_of(int k, const Params& p) {
   return i < n ? base + i : -1;
 }
 
-// Number of K/V tiles a Q tile starting at `row_start` visits (0 if it holds no row < N).
+// Number of K/V tiles (BN keys each) a 128-row Q tile starting at `row_start` visits (0 if
+// it holds no row < N).
+template <int BN = kBlockN>
 __device__ __forceinline__ int tiles_for(int row_start, const Params& p) {
   if (row_start >= p.N) return 0;
   if (!p.causal) return p.nkv;
-  const int t = row_start / kBlockN + 1;  // tiles up to and including the diagonal one
+  const int t = (row_start + kBlockM - 1) / BN + 1;  // tiles up to and including the diagonal one
   return t < p.nkv ? t : p.nkv;
 }
 
@@ -166,12 +176,12 @@ struct Item {
 };
 
 // SPLIT = false compiles the unsplit kernel: an item is a whole unit, k0 = 0.
-template <bool SPLIT = true>
+template <bool SPLIT = true, int BN = kBlockN>
 __device__ __forceinline__ void item_coords(int w, const Params& p, Item& it) {
   const int u = SPLIT ? w / p.splits : w;
   const int sp = SPLIT ? w - u * p.splits : 0;
   unit_coords(u, p, it.bh, it.row0);
-  const int n0 = tiles_for(it.row0, p), n1 = tiles_for(it.row0 + kBlockM, p);
+  const int n0 = tiles_for<BN>(it.row0, p), n1 = tiles_for<BN>(it.row0 + kBlockM, p);
   const int n = n0 > n1 ? n0 : n1;
   it.k0 = SPLIT ? sp * n / p.splits : 0;
   it.k1 = SPLIT ? (sp + 1) * n / p.splits : n;
@@ -187,6 +197,13 @@ __device__ __forceinline__ void raise_abort(Barriers& b) {
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p,
                                          Barriers& b) {
   return mbar_wait_bounded(bar, parity, p.budget, &b.abort);
+}
+
+// A bounded wait taken by a whole warp: true only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
+                                          Barriers& b) {
+  const bool ok = wait_bar(bar, parity, p, b);
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // Time-bounded wait that ignores the abort flag (used to drain in-flight async work).
@@ -205,10 +222,10 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* ptr) {
 // ------------------------------------------------------------------------------------
 // TMA producer (one lane)
 // ------------------------------------------------------------------------------------
-template <int HD, bool SPLIT>
+template <int HD, int BN, bool SPLIT>
 __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                           uint8_t* sQ, uint8_t* sRing, Barriers& b, const Params& p) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, BN>;
   prefetch_tmap(tmQ);
   prefetch_tmap(tmK);
   prefetch_tmap(tmV);
@@ -219,7 +236,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
     const int u = item_of(k, p);
     if (u < 0) continue;
     Item it;
-    item_coords<SPLIT>(u, p, it);
+    item_coords<SPLIT, BN>(u, p, it);
     if (it.k1 <= it.k0) continue;  // an empty KV range (more splits than tiles)
     const int bh = it.bh, row0 = it.row0;
     // Q smem is free once the previous item's last S MMA has completed
@@ -238,11 +255,11 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
         if (skip) {
           skipped = ring;
         } else {
-          mbar_arrive_expect_tx(&b.slot_full[slot], C::TILE_BYTES);
+          mbar_arrive_expect_tx(&b.slot_full[slot], C::KV_TILE_BYTES);
           const CUtensorMap* m = kv == 0 ? tmK : tmV;
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sRing + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, m, &b.slot_full[slot],
-                        c * C::W, j * kBlockN, bh);
+            tma_load_3d(sRing + slot * C::KV_TILE_BYTES + c * C::KV_CHUNK_BYTES, m,
+                        &b.slot_full[slot], c * C::W, j * BN, bh);
         }
         ++ring;
       }
@@ -259,35 +276,35 @@ drain:
 }
 
 // ------------------------------------------------------------------------------------
-// MMA issuer (one lane)
+// MMA issuer (one whole warp; one elected lane issues each MMA and commit)
 // ------------------------------------------------------------------------------------
-template <int HD>
+template <int HD, int BN = kBlockN, bool WARP = true>
 __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_addr, uint32_t k_addr) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, BN>;
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     const int ch = (kk * 16) / C::W, off = ((kk * 16) % C::W) * 2;
     const uint64_t a = smem_desc(q_addr + ch * C::CHUNK_BYTES + off, 16, 8 * C::SWB, C::SWZ);
-    const uint64_t bd = smem_desc(k_addr + ch * C::CHUNK_BYTES + off, 16, 8 * C::SWB, C::SWZ);
-    mma_bf16_ss(tmem_d, a, bd, C::IDESC_S, kk > 0);
+    const uint64_t bd = smem_desc(k_addr + ch * C::KV_CHUNK_BYTES + off, 16, 8 * C::SWB, C::SWZ);
+    mma_bf16_ss<WARP>(tmem_d, a, bd, C::IDESC_S, kk > 0);
   }
 }
 
-template <int HD>
+template <int HD, int BN = kBlockN, bool WARP = true>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
                                          bool accumulate) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, BN>;
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+  for (int kk = 0; kk < BN / 16; ++kk) {
     // V tile is [key][d]: the B operand (K = keys, N = d) is MN-major
-    const uint64_t bd = smem_desc(v_addr + kk * 16 * C::SWB, C::CHUNK_BYTES, 8 * C::SWB, C::SWZ);
-    mma_bf16_ts(tmem_o, tmem_p + kk * 8, bd, C::IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+    const uint64_t bd = smem_desc(v_addr + kk * 16 * C::SWB, C::KV_CHUNK_BYTES, 8 * C::SWB, C::SWZ);
+    mma_bf16_ts<WARP>(tmem_o, tmem_p + kk * 8, bd, C::IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
-template <int HD, bool SPLIT>
+template <int HD, int BN, bool SPLIT>
 __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b, const Params& p) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, BN>;
   uint32_t ring = 0, units = 0;
   uint32_t p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
   const uint32_t q_addr[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE_BYTES)};
@@ -297,47 +314,47 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
     const int u = item_of(k, p);
     if (u < 0) continue;
     Item it;
-    item_coords<SPLIT>(u, p, it);
+    item_coords<SPLIT, BN>(u, p, it);
     if (it.k1 <= it.k0) continue;
     const int k0 = it.k0, k1 = it.k1;
-    if (!wait_bar(&b.q_full, units & 1, p, b)) goto fail;
+    if (!warp_wait(&b.q_full, units & 1, p, b)) goto fail;
     ++units;
     uint32_t ks = ring % C::NSLOT;
-    if (!wait_bar(&b.slot_full[ks], (ring / C::NSLOT) & 1, p, b)) goto fail;
+    if (!warp_wait(&b.slot_full[ks], (ring / C::NSLOT) & 1, p, b)) goto fail;
     ++ring;
     tc_fence_after_sync();
     for (int t = 0; t < 2; ++t)
       if (it.e[t] > k0) {
-        issue_s<HD>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::TILE_BYTES);
+        issue_s<HD, BN>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::KV_TILE_BYTES);
         mma_commit(&b.s_full[t]);
       }
     mma_commit(&b.slot_empty[ks]);
     if (k1 - k0 == 1) mma_commit(&b.q_empty);
     for (int j = k0; j < k1; ++j) {
       const uint32_t vs = ring % C::NSLOT;
-      if (!wait_bar(&b.slot_full[vs], (ring / C::NSLOT) & 1, p, b)) goto fail;
+      if (!warp_wait(&b.slot_full[vs], (ring / C::NSLOT) & 1, p, b)) goto fail;
       ++ring;
       const bool next = j + 1 < k1;
       if (next) {
         ks = ring % C::NSLOT;
-        if (!wait_bar(&b.slot_full[ks], (ring / C::NSLOT) & 1, p, b)) goto fail;
+        if (!warp_wait(&b.slot_full[ks], (ring / C::NSLOT) & 1, p, b)) goto fail;
         ++ring;
       }
       tc_fence_after_sync();
       for (int t = 0; t < 2; ++t) {
         if (j < it.e[t]) {
           if (j == k0) {  // O_t must have been read out by the previous item's epilogue
-            if (!wait_bar(&b.o_empty[t], (oe_cnt[t] & 1) ^ 1, p, b)) goto fail;
+            if (!warp_wait(&b.o_empty[t], (oe_cnt[t] & 1) ^ 1, p, b)) goto fail;
             ++oe_cnt[t];
           }
-          if (!wait_bar(&b.p_full[t], p_cnt[t] & 1, p, b)) goto fail;
+          if (!warp_wait(&b.p_full[t], p_cnt[t] & 1, p, b)) goto fail;
           ++p_cnt[t];
           tc_fence_after_sync();
-          issue_pv<HD>(tmem + col_o[t], tmem + col_s[t], ring_addr + vs * C::TILE_BYTES, j > k0);
+          issue_pv<HD, BN>(tmem + col_o[t], tmem + col_s[t], ring_addr + vs * C::KV_TILE_BYTES, j > k0);
           if (j == it.e[t] - 1) mma_commit(&b.o_full[t]);
         }
         if (next && j + 1 < it.e[t]) {
-          issue_s<HD>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::TILE_BYTES);
+          issue_s<HD, BN>(tmem + col_s[t], q_addr[t], ring_addr + ks * C::KV_TILE_BYTES);
           mma_commit(&b.s_full[t]);
         }
       }
@@ -357,11 +374,5 @@ drain:
   drain_bar(&b.drain, 0, p);
 }
 
-// A bounded wait taken by a whole warp: true only if every lane saw the phase complete.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
-                                          Barriers& b) {
-  const bool ok = wait_bar(bar, parity, p, b);
-  return __all_sync(0xFFFFFFFFu, ok);
-}
 
 }  // namespace fa_sm103

@@ -8,8 +8,8 @@
 // What differs is how the softmax is laid out on the SM:
 //   * Warps (512 threads = 4 warpgroups): warpgroup 0 = softmax for Q tile 0,
 //     warpgroup 1 = softmax for Q tile 1, warpgroup 2 = epilogue (O / l, logsumexp,
-//     stores), warp 12 = tcgen05 MMA issuer (one lane), warp 13 = TMA producer (one
-//     lane), warps 14-15 idle.  Warp w reads TMEM lane quadrant w % 4, so every SM
+//     stores), warp 12 = tcgen05 MMA issuer (the whole warp; one elected lane issues),
+//     warp 13 = TMA producer (one lane), warps 14-15 idle.  Warp w reads TMEM lane quadrant w % 4, so every SM
 //     sub-partition holds one warp of each role.
 //   * Each softmax thread owns one query row and all 128 key columns of a score tile:
 //     the row maximum needs no exchange between threads.  Registers are moved to the
@@ -40,8 +40,8 @@ constexpr int kLoadWarpR = 13;
 // and were measured to cost ~500 cycles on the path S ready -> P ready.
 constexpr uint32_t kRowWarpsPerTile = 4;
 // Dynamic shared memory of a launch: split launches add the epilogue's store blocks.
-template <int HD, bool SPLIT>
-constexpr int row_kernel_smem() { return Cfg<HD>::SMEM_BYTES + (SPLIT ? 4 * 4096 : 0); }
+template <int HD, int BN, bool SPLIT>
+constexpr int row_kernel_smem() { return Cfg<HD, BN>::SMEM_BYTES + (SPLIT ? 4 * 4096 : 0); }
 constexpr uint32_t kEpilogueWarps = 4;
 // Registers per thread the kernel must be compiled to (512 threads x 128 = the SM's 64K),
 // and the per-warpgroup shares setmaxnreg moves them to.  The shares add up to exactly
@@ -61,14 +61,14 @@ struct RowStats {
   float l_round[2][2][kBlockM];
 };
 
-// Row maximum of the 128 raw scores (columns > lim masked when MASK).
-template <bool MASK>
-__device__ __forceinline__ float row_max128(const uint32_t (&s)[128], int lim) {
+// Row maximum of the BN raw scores (columns > lim masked when MASK).
+template <int BN, bool MASK>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[BN], int lim) {
   float m[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) m[k] = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 128; i += 16) {
+  for (int i = 0; i < BN; i += 16) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       float x0 = __uint_as_float(s[i + 2 * k]), x1 = __uint_as_float(s[i + 2 * k + 1]);
@@ -84,10 +84,10 @@ __device__ __forceinline__ float row_max128(const uint32_t (&s)[128], int lim) {
 
 // P = 2^(s*c - m) for columns [32*part, 32*part + 32), packed to bf16x2 into
 // pk[16*part .. 16*part + 15].  Returns the sum of the fp32 P; two accumulators keep
-// the addition chain short.  The sum of the rounded P is taken later (rounded_sum64),
+// the addition chain short.  The sum of the rounded P is taken later (rounded_sum),
 // after P has been handed to the MMA.
-template <bool MASK>
-__device__ __forceinline__ float exp_pack32_row(const uint32_t (&s)[128], uint32_t (&pk)[64],
+template <int BN, bool MASK>
+__device__ __forceinline__ float exp_pack32_row(const uint32_t (&s)[BN], uint32_t (&pk)[BN / 2],
                                                 int part, uint64_t c2, uint64_t negm2, int lim) {
   uint64_t esum[2] = {0, 0};
 #pragma unroll
@@ -111,18 +111,19 @@ __device__ __forceinline__ float exp_pack32_row(const uint32_t (&s)[128], uint32
   return (e0 + e1) + (e2 + e3);
 }
 
-// Sum of the 128 bf16 values packed in pk (exact widening, fp32 additions).
-__device__ __forceinline__ float rounded_sum64(const uint32_t (&pk)[64]) {
+// Sum of the BN bf16 values packed in pk (exact widening, fp32 additions).
+template <int NW>
+__device__ __forceinline__ float rounded_sum(const uint32_t (&pk)[NW]) {
   float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < 64; ++i) a[i & 3] = add_bf16x2_to_f32(a[i & 3], pk[i]);
+  for (int i = 0; i < NW; ++i) a[i & 3] = add_bf16x2_to_f32(a[i & 3], pk[i]);
   return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
 // ------------------------------------------------------------------------------------
 // softmax (warpgroups 0 and 1): thread = one query row of Q tile t = warp / 4
 // ------------------------------------------------------------------------------------
-template <int HD, bool SPLIT>
+template <int HD, int BN, bool SPLIT>
 __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const Params& p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = warp >> 2, wq = warp & 3;
@@ -137,7 +138,7 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
     const int u = item_of(k, p);
     if (u < 0) continue;
     Item it;
-    item_coords<SPLIT>(u, p, it);
+    item_coords<SPLIT, BN>(u, p, it);
     const int e_t = it.end(t);
     if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
     const int row = it.row0 + t * kBlockM + lrow;
@@ -149,14 +150,14 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
       if (!warp_wait(&b.s_full[t], s_cnt & 1, p, b)) goto fail;
       ++s_cnt;
       tc_fence_after_sync();
-      uint32_t s[128];
-      tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
-      tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&s[64]));
+      uint32_t s[BN];
+#pragma unroll
+      for (int h = 0; h < BN; h += 64) tmem_ld_x64(tS + h, *reinterpret_cast<uint32_t(*)[64]>(&s[h]));
       tmem_wait_ld(s);
-      const int kv0 = j * kBlockN;
+      const int kv0 = j * BN;
       const int lim = last_key - kv0;  // last admissible column of the tile
-      const bool warp_mask = __any_sync(0xFFFFFFFFu, kv0 + kBlockN - 1 > last_key);
-      const float mx = warp_mask ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
+      const bool warp_mask = __any_sync(0xFFFFFFFFu, kv0 + BN - 1 > last_key);
+      const float mx = warp_mask ? row_max<BN, true>(s, lim) : row_max<BN, false>(s, lim);
       const float mt = mx * c;
       const bool need = mt > m_ref + kRescaleLog2;  // also true while m_ref is -inf
       const bool warp_rescale = __any_sync(0xFFFFFFFFu, need);
@@ -168,12 +169,12 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
         l_round *= alpha;
       }
       const uint64_t negm2 = f32x2(-m_ref, -m_ref);
-      uint32_t pk[64];  // P as bf16 pairs, kept for the rounded row sum below
+      uint32_t pk[BN / 2];  // P as bf16 pairs, kept for the rounded row sum below
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        l_exact += warp_mask ? exp_pack32_row<true>(s, pk, part, c2, negm2, lim)
-                             : exp_pack32_row<false>(s, pk, part, c2, negm2, lim);
-        // P (bf16 pairs) over the first 64 columns of S
+      for (int part = 0; part < BN / 32; ++part) {
+        l_exact += warp_mask ? exp_pack32_row<BN, true>(s, pk, part, c2, negm2, lim)
+                             : exp_pack32_row<BN, false>(s, pk, part, c2, negm2, lim);
+        // P (bf16 pairs) over the first BN/2 columns of S
         tmem_st_x16(tS + 16 * part, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * part]));
       }
       if (warp_rescale && j > it.k0) {
@@ -194,7 +195,7 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.p_full[t]);
       // off the critical path: the MMA already has P, the next S is not ready yet
-      l_round += rounded_sum64(pk);
+      l_round += rounded_sum(pk);
     }
     {
       // hand the row statistics to the epilogue (buffer = parity of this tile's units)
@@ -261,7 +262,7 @@ __device__ __forceinline__ void flush_rows(uint32_t scratch, int lane, uint8_t* 
 // l_round rounded to bf16 (or, for a split item, the normalised fp32 partial O), and
 // lse = (m_ref + log2 l_exact) ln 2.
 // ------------------------------------------------------------------------------------
-template <int HD, bool SPLIT>
+template <int HD, int BN, bool SPLIT>
 __device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Params& p,
                               uint8_t* sScratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -274,7 +275,7 @@ __device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Pa
     const int u = item_of(k, p);
     if (u < 0) continue;
     Item it;
-    item_coords<SPLIT>(u, p, it);
+    item_coords<SPLIT, BN>(u, p, it);
 #pragma unroll 1
     for (int t = 0; t < 2; ++t) {
       if (it.end(t) <= it.k0) continue;
@@ -350,17 +351,17 @@ fail:
 }
 
 // ------------------------------------------------------------------------------------
-template <int HD, bool SPLIT>
+template <int HD, int BN, bool SPLIT>
 __global__ void __launch_bounds__(kThreadsR, 1)
     fa_fwd_row_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const Params p) {
   static_assert(HD <= 128, "the row kernel serves head dims 16..128");
-  using C = Cfg<HD>;
+  using C = Cfg<HD, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + C::SMEM_Q;
-  uint8_t* sScratch = sRing + C::NSLOT * C::TILE_BYTES;  // split launches: epilogue store blocks
+  uint8_t* sScratch = sRing + C::NSLOT * C::KV_TILE_BYTES;  // split launches: epilogue store blocks
   __shared__ Barriers b;
   __shared__ RowStats rs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -395,19 +396,19 @@ __global__ void __launch_bounds__(kThreadsR, 1)
 
   if (warp < kEpilogueWarp0) {
     setmaxnreg_inc<kRegsSoftmax>();
-    softmax_row_role<HD, SPLIT>(tmem, b, rs, p);
+    softmax_row_role<HD, BN, SPLIT>(tmem, b, rs, p);
     setmaxnreg_dec<128>();
   } else if (warp < kMmaWarpR) {
     setmaxnreg_dec<kRegsEpilogue>();
-    epilogue_role<HD, SPLIT>(tmem, b, rs, p, sScratch);
+    epilogue_role<HD, BN, SPLIT>(tmem, b, rs, p, sScratch);
     setmaxnreg_inc<128>();
   } else {
     setmaxnreg_dec<kRegsControl>();
     if (warp == kMmaWarpR) {
-      if (lane == 0) mma_role<HD, SPLIT>(sQ, sRing, tmem, b, p);
+      mma_role<HD, BN, SPLIT>(sQ, sRing, tmem, b, p);
       __syncwarp();
     } else if (warp == kLoadWarpR) {
-      if (lane == 0) load_role<HD, SPLIT>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
+      if (lane == 0) load_role<HD, BN, SPLIT>(&tmQ, &tmK, &tmV, sQ, sRing, b, p);
       __syncwarp();
     }
     setmaxnreg_inc<128>();

@@ -49,7 +49,8 @@ __device__ __forceinline__ void load_partial(const float* src, float (&x)[E]) {
 // UNIT_ROWS: the query rows of the split kernel's work unit -- kUnitRows (two-tile
 // kernel: a piece may hold no admissible key for tile 0's rows) or kUnitRows1 (one-tile
 // kernel: every non-empty piece holds some).
-template <int HD, int UNIT_ROWS, int NP>
+// BN: the key-tile width of the split kernel (its pieces are ranges of key tiles).
+template <int HD, int UNIT_ROWS, int NP, int BN = kBlockN>
 __global__ void __launch_bounds__(kMergeThreads)
     fa_merge_kernel(const Params p) {
   static_assert(HD <= 256, "head dims 16 to 256");
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kMergeThreads)
       bool holds;
       if constexpr (UNIT_ROWS == kUnitRows) {
         Item it;
-        item_coords<true>(static_cast<int>(base) + sp, p, it);
+        item_coords<true, BN>(static_cast<int>(base) + sp, p, it);
         holds = it.end(t) > it.k0;
       } else {
         int ibh, irow0, k0, k1;
