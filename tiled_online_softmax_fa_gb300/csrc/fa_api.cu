@@ -489,16 +489,17 @@ int grid_for(const DeviceState& dev, const fa_fwd_options* opts, int items) {
 // 2 or 8 pieces are loaded up front (the smallest bucket that holds `splits`).
 template <int HD, int UNIT_ROWS, int BN = fa_sm103::kBlockN>
 int launch_merge(const fa_sm103::Params& p, int64_t BH, int64_t N, cudaStream_t stream) {
-  const int64_t warps = BH * N;
-  const unsigned blocks = static_cast<unsigned>((warps + fa_sm103::kMergeThreads / 32 - 1) /
-                                                (fa_sm103::kMergeThreads / 32));
-  constexpr int T = fa_sm103::kMergeThreads;
-  if (p.splits <= 2)
-    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 2, BN><<<blocks, T, 0, stream>>>(p);
+  constexpr int T = fa_sm103::kMergeThreads, WPB = T / 32;
+  const int64_t rows = BH * N;
+  auto blocks = [&](int rows_per_warp) {
+    return static_cast<unsigned>((rows + int64_t{WPB} * rows_per_warp - 1) / (int64_t{WPB} * rows_per_warp));
+  };
+  if (p.splits <= 2)  // (two rows per warp measured slower: 28.3 vs 25.8 us for 65,536 rows)
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 2, BN, 1><<<blocks(1), T, 0, stream>>>(p);
   else if (p.splits <= 8)
-    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 8, BN><<<blocks, T, 0, stream>>>(p);
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 8, BN, 1><<<blocks(1), T, 0, stream>>>(p);
   else
-    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 0, BN><<<blocks, T, 0, stream>>>(p);
+    fa_sm103::fa_merge_kernel<HD, UNIT_ROWS, 0, BN, 1><<<blocks(1), T, 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error("merge kernel launch", e);
   return FA_OK;

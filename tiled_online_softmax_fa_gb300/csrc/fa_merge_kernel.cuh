@@ -35,6 +35,32 @@ __device__ __forceinline__ void load_partial(const float* src, float (&x)[E]) {
   }
 }
 
+// The merge of one query row, in two halves so that a warp can put the loads of several
+// rows in flight before it needs any of them (merge_load, then merge_finish).
+struct MergeRow {
+  int bh, row, rin, t;
+  size_t base;  // the row's first piece (item index)
+  bool valid;   // row < BH * N
+};
+
+template <int UNIT_ROWS>
+__device__ __forceinline__ MergeRow merge_row(const Params& p, int64_t gw) {
+  MergeRow r;
+  r.valid = gw < static_cast<int64_t>(p.BH) * p.N;
+  if (!r.valid) gw = 0;
+  r.bh = static_cast<int>(gw / p.N);
+  r.row = static_cast<int>(gw - static_cast<int64_t>(r.bh) * p.N);
+  const int qb = r.row / UNIT_ROWS;
+  r.rin = r.row - qb * UNIT_ROWS;
+  r.t = r.rin / kBlockM;
+  // unit of (bh, qb): the inverse of unit_coords
+  const int g = r.bh / p.group_heads, first = g * p.group_heads;
+  const int heads = (p.BH - first) < p.group_heads ? (p.BH - first) : p.group_heads;
+  const int u = g * p.group_heads * p.nqb + (p.nqb - 1 - qb) * heads + (r.bh - first);
+  r.base = static_cast<size_t>(u) * p.splits;
+  return r;
+}
+
 // One warp per query row.  The row's pieces are found in the lanes (lane s holds piece s
 // and s + 32): their lse values give the row maximum and the weights exp(lse_s - m)
 // through two warp reductions.  Each lane reads its E columns of every piece and writes
@@ -43,117 +69,119 @@ __device__ __forceinline__ void load_partial(const float* src, float (&x)[E]) {
 // loaded before the lse values are known, so a row costs one memory round trip instead
 // of two, and the registers for them are sized to NP, so launches of few pieces keep
 // more rows in flight per SM (memory-bound: bytes in flight set the rate); NP = 0 loads
-// each piece once its weight is known.  A piece without an admissible key for the row
-// (its key range starts past the row's diagonal tile, its partial never written) has
-// weight 0 and its loaded values are not used.
+// each piece once its weight is known.  With R = 2 a warp merges two consecutive rows,
+// all of their loads issued before either row is finished.  A piece without an
+// admissible key for the row (its key range starts past the row's diagonal tile, its
+// partial never written) has weight 0 and its loaded values are not used.
 // UNIT_ROWS: the query rows of the split kernel's work unit -- kUnitRows (two-tile
 // kernel: a piece may hold no admissible key for tile 0's rows) or kUnitRows1 (one-tile
-// kernel: every non-empty piece holds some).
-// BN: the key-tile width of the split kernel (its pieces are ranges of key tiles).
-template <int HD, int UNIT_ROWS, int NP, int BN = kBlockN>
+// kernel: every non-empty piece holds some).  BN: the key-tile width of the split kernel
+// (its pieces are ranges of key tiles).
+template <int HD, int UNIT_ROWS, int NP, int BN = kBlockN, int R = 1>
 __global__ void __launch_bounds__(kMergeThreads)
     fa_merge_kernel(const Params p) {
   static_assert(HD <= 256, "head dims 16 to 256");
   constexpr int E = HD >= 256 ? 8 : (HD >= 128 ? 4 : (HD >= 64 ? 2 : 1));  // per lane
   constexpr int kLanes = HD / E;                          // lanes that hold columns
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
-  if (gw >= static_cast<int64_t>(p.BH) * p.N) return;
-  const int bh = static_cast<int>(gw / p.N), row = static_cast<int>(gw - static_cast<int64_t>(bh) * p.N);
-  const int qb = row / UNIT_ROWS, rin = row - qb * UNIT_ROWS, t = rin / kBlockM;
-  // unit of (bh, qb): the inverse of unit_coords
-  const int g = bh / p.group_heads, first = g * p.group_heads;
-  const int heads = (p.BH - first) < p.group_heads ? (p.BH - first) : p.group_heads;
-  const int u = g * p.group_heads * p.nqb + (p.nqb - 1 - qb) * heads + (bh - first);
-  const size_t base = static_cast<size_t>(u) * p.splits;
-  const bool active = lane < kLanes;
   constexpr bool eager = NP > 0;
-  float xe[eager ? NP : 1][E];
-  if (eager && active) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw0 = (static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5)) * R;
+  const bool active = lane < kLanes;
+  MergeRow mr[R];
+  float xe[R][eager ? NP : 1][E];
 #pragma unroll
-    for (int sp = 0; sp < (eager ? NP : 1); ++sp)
-      if (sp < p.splits)
-        load_partial<E>(p.ws_o + ((base + sp) * UNIT_ROWS + rin) * HD + lane * E, xe[sp]);
+  for (int r = 0; r < R; ++r) {
+    mr[r] = merge_row<UNIT_ROWS>(p, gw0 + r);
+    if (eager && active && mr[r].valid) {
+#pragma unroll
+      for (int sp = 0; sp < (eager ? NP : 1); ++sp)
+        if (sp < p.splits)
+          load_partial<E>(p.ws_o + ((mr[r].base + sp) * UNIT_ROWS + mr[r].rin) * HD + lane * E,
+                          xe[r][sp]);
+    }
   }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (!mr[r].valid) continue;  // warp-uniform
+    const MergeRow& m0 = mr[r];
+    // pieces s = lane and lane + 32: their lse, or -inf without an admissible key
+    float ls[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int sp = lane + 32 * h;
+      if (sp < p.splits) {
+        bool holds;
+        if constexpr (UNIT_ROWS == kUnitRows) {
+          Item it;
+          item_coords<true, BN>(static_cast<int>(m0.base) + sp, p, it);
+          holds = it.end(m0.t) > it.k0;
+        } else {
+          int ibh, irow0, k0, k1;
+          one::item_coords1<true>(static_cast<int>(m0.base) + sp, p, ibh, irow0, k0, k1);
+          holds = k1 > k0;
+        }
+        if (holds) ls[h] = p.ws_lse[(m0.base + sp) * UNIT_ROWS + m0.rin];
+      }
+    }
+    float m = fmaxf(ls[0], ls[1]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    float w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) w[h] = ls[h] == -INFINITY ? 0.f : expf(ls[h] - m);
+    float denom = w[0] + w[1];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xFFFFFFFFu, denom, off);
 
-  // pieces s = lane and lane + 32: their lse, or -inf without an admissible key
-  float ls[2] = {-INFINITY, -INFINITY};
+    float acc[E];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int sp = lane + 32 * h;
-    if (sp < p.splits) {
-      bool holds;
-      if constexpr (UNIT_ROWS == kUnitRows) {
-        Item it;
-        item_coords<true, BN>(static_cast<int>(base) + sp, p, it);
-        holds = it.end(t) > it.k0;
-      } else {
-        int ibh, irow0, k0, k1;
-        one::item_coords1<true>(static_cast<int>(base) + sp, p, ibh, irow0, k0, k1);
-        holds = k1 > k0;
+    for (int i = 0; i < E; ++i) acc[i] = 0.f;
+    if constexpr (eager) {
+#pragma unroll
+      for (int sp = 0; sp < NP; ++sp) {
+        if (sp >= p.splits) break;
+        const float wgt = __shfl_sync(0xFFFFFFFFu, w[0], sp);
+        if (wgt != 0.f && active) {
+#pragma unroll
+          for (int i = 0; i < E; ++i) acc[i] += wgt * xe[r][sp][i];
+        }
       }
-      if (holds) ls[h] = p.ws_lse[(base + sp) * UNIT_ROWS + rin];
-    }
-  }
-  float m = fmaxf(ls[0], ls[1]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-  float w[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) w[h] = ls[h] == -INFINITY ? 0.f : expf(ls[h] - m);
-  float denom = w[0] + w[1];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xFFFFFFFFu, denom, off);
-
-  float acc[E];
-#pragma unroll
-  for (int i = 0; i < E; ++i) acc[i] = 0.f;
-  if constexpr (eager) {
-#pragma unroll
-    for (int sp = 0; sp < NP; ++sp) {
-      if (sp >= p.splits) break;
-      const float wgt = __shfl_sync(0xFFFFFFFFu, w[0], sp);
-      if (wgt != 0.f && active) {
-#pragma unroll
-        for (int i = 0; i < E; ++i) acc[i] += wgt * xe[sp][i];
-      }
-    }
-  } else {
-#pragma unroll 4
-    for (int sp = 0; sp < p.splits; ++sp) {
-      const float wgt = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w[0] : w[1], sp & 31);
-      if (wgt != 0.f && active) {
-        float x[E];
-        load_partial<E>(p.ws_o + ((base + sp) * UNIT_ROWS + rin) * HD + lane * E, x);
-#pragma unroll
-        for (int i = 0; i < E; ++i) acc[i] += wgt * x[i];
-      }
-    }
-  }
-  const float inv = 1.f / denom;
-  if (active) {
-    __nv_bfloat16* dst = p.o + (static_cast<size_t>(bh) * p.N + row) * HD + lane * E;
-    if constexpr (E == 8) {
-      uint4 v;
-      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-      v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(dst) = v;
-    } else if constexpr (E == 4) {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-      uint2 v;
-      v.x = *reinterpret_cast<const uint32_t*>(&lo);
-      v.y = *reinterpret_cast<const uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(dst) = v;
-    } else if constexpr (E == 2) {
-      *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
     } else {
-      dst[0] = __float2bfloat16_rn(acc[0] * inv);
+#pragma unroll 4
+      for (int sp = 0; sp < p.splits; ++sp) {
+        const float wgt = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w[0] : w[1], sp & 31);
+        if (wgt != 0.f && active) {
+          float x[E];
+          load_partial<E>(p.ws_o + ((m0.base + sp) * UNIT_ROWS + m0.rin) * HD + lane * E, x);
+#pragma unroll
+          for (int i = 0; i < E; ++i) acc[i] += wgt * x[i];
+        }
+      }
     }
+    const float inv = 1.f / denom;
+    if (active) {
+      __nv_bfloat16* dst = p.o + (static_cast<size_t>(m0.bh) * p.N + m0.row) * HD + lane * E;
+      if constexpr (E == 8) {
+        uint4 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4*>(dst) = v;
+      } else if constexpr (E == 4) {
+        uint2 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = v;
+      } else if constexpr (E == 2) {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      } else {
+        dst[0] = __float2bfloat16_rn(acc[0] * inv);
+      }
+    }
+    if (lane == 0 && p.lse != nullptr)
+      p.lse[static_cast<size_t>(m0.bh) * p.N + m0.row] = m + logf(denom);
   }
-  if (lane == 0 && p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.N + row] = m + logf(denom);
 }
 
 }  // namespace fa_sm103
