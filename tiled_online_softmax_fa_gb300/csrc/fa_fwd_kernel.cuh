@@ -70,10 +70,20 @@ struct Cfg {
   static constexpr int NSLOT = (HD == 128 && BN == 128) ? 4
                                : ((128 * 1024) / KV_TILE_BYTES < 8 ? (128 * 1024) / KV_TILE_BYTES : 8);
   static constexpr int SMEM_Q = 2 * TILE_BYTES;
-  static constexpr int SMEM_BYTES = SMEM_Q + NSLOT * KV_TILE_BYTES + 1024;  // + alignment pad
+  // Two-tile kernel, head dims up to 64: the PV MMA runs NO = HD + 16 output columns, the
+  // last 16 reading a block of bf16 ones placed after the ring (ONES_BYTES, one V column
+  // chunk), so O's column HD accumulates the row sum of the rounded P.  The one-tile
+  // kernel sizes its own shared memory and does not use these.
+  static constexpr bool ONES = HD <= 64;
+  static constexpr int NO = ONES ? HD + 16 : HD;
+  static constexpr int ONES_BYTES = ONES ? KV_CHUNK_BYTES : 0;
+  static constexpr int SMEM_BYTES = SMEM_Q + NSLOT * KV_TILE_BYTES + ONES_BYTES + 1024;  // + alignment pad
   static constexpr uint32_t SWZ = swizzle_code(SWB);
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(kBlockM, BN, false);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(kBlockM, HD, true);
+  static constexpr uint32_t IDESC_O_ONES = idesc_bf16_f32(kBlockM, NO, true);
+  // the ones block's offset from any V tile must fit the descriptor's 14-bit stride field
+  static_assert(!ONES || NSLOT * KV_TILE_BYTES < (1 << 18), "ones block out of descriptor reach");
 };
 
 struct Params {
@@ -290,15 +300,20 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_addr, uint32
   }
 }
 
+// ones_addr != 0 (two-tile kernel, Cfg::ONES): N = HD + 16, and B's second column chunk
+// comes from the ones block: its offset from the V tile is passed as the descriptor's
+// stride between column chunks, so the MMA reads HD columns of V, then 16 columns of ones.
 template <int HD, int BN = kBlockN, bool WARP = true>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
-                                         bool accumulate) {
+                                         bool accumulate, uint32_t ones_addr = 0) {
   using C = Cfg<HD, BN>;
+  const uint32_t lbo = ones_addr ? ones_addr - v_addr : C::KV_CHUNK_BYTES;
+  const uint32_t idesc = ones_addr ? C::IDESC_O_ONES : C::IDESC_O;
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
     // V tile is [key][d]: the B operand (K = keys, N = d) is MN-major
-    const uint64_t bd = smem_desc(v_addr + kk * 16 * C::SWB, C::KV_CHUNK_BYTES, 8 * C::SWB, C::SWZ);
-    mma_bf16_ts<WARP>(tmem_o, tmem_p + kk * 8, bd, C::IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+    const uint64_t bd = smem_desc(v_addr + kk * 16 * C::SWB, lbo, 8 * C::SWB, C::SWZ);
+    mma_bf16_ts<WARP>(tmem_o, tmem_p + kk * 8, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -350,7 +365,8 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
           if (!warp_wait(&b.p_full[t], p_cnt[t] & 1, p, b)) goto fail;
           ++p_cnt[t];
           tc_fence_after_sync();
-          issue_pv<HD, BN>(tmem + col_o[t], tmem + col_s[t], ring_addr + vs * C::KV_TILE_BYTES, j > k0);
+          issue_pv<HD, BN>(tmem + col_o[t], tmem + col_s[t], ring_addr + vs * C::KV_TILE_BYTES, j > k0,
+                           C::ONES ? ring_addr + C::NSLOT * C::KV_TILE_BYTES : 0u);
           if (j == it.e[t] - 1) mma_commit(&b.o_full[t]);
         }
         if (next && j + 1 < it.e[t]) {

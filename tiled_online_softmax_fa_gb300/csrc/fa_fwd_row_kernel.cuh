@@ -21,9 +21,12 @@
 //     double-buffered by unit parity.
 // Numerics are those of fa_fwd_kernel: exp2 with the scale folded into one FMA, lazy
 // rescale (threshold 8 in log2 units), P rounded to bf16 for the PV MMA, l_round (sum
-// of the rounded P) normalises O, l_exact gives the logsumexp.  l_round is summed from
-// the packed P after P has been handed to the MMA, so it stays off the chain
-// S ready -> P ready that the tensor core waits on.
+// of the rounded P) normalises O, l_exact gives the logsumexp.  Up to head dim 128,
+// l_round is summed from the packed P after P has been handed to the MMA, so it stays
+// off the chain S ready -> P ready that the tensor core waits on.  Up to head dim 64 the
+// tensor core sums it: the PV MMA runs HD + 16 output columns, the extra 16 reading a
+// shared-memory block of bf16 ones, so O's column HD accumulates sum_k P_k in fp32 like
+// the rest of O (TMEM has the room there), rescaled with O and read by the epilogue.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -179,9 +182,10 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
       }
       if (warp_rescale && j > it.k0) {
         // PV_t(j-1) has completed (S_t(j) was issued after it) and PV_t(j) waits for
-        // this thread's arrival below: rescale this row of O in place.
+        // this thread's arrival below: rescale this row of O in place (with the ones
+        // columns, which hold the row sum, at head dims up to 64).
 #pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
+        for (int c0 = 0; c0 < Cfg<HD, BN>::NO; c0 += 32) {
           uint32_t o[32];
           tmem_ld_x32(tO + c0, o);
           tmem_wait_ld(o);
@@ -195,7 +199,7 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.p_full[t]);
       // off the critical path: the MMA already has P, the next S is not ready yet
-      l_round += rounded_sum(pk);
+      if constexpr (!Cfg<HD, BN>::ONES) l_round += rounded_sum(pk);
     }
     {
       // hand the row statistics to the epilogue (buffer = parity of this tile's units)
@@ -285,10 +289,16 @@ __device__ void epilogue_role(uint32_t tmem, Barriers& b, RowStats& rs, const Pa
       if (!warp_wait(&b.stats_full[t][par], (c >> 1) & 1, p, b)) goto fail;
       const float m_ref = rs.m_ref[t][par][lrow];
       const float l_exact = rs.l_exact[t][par][lrow];
-      const float l_round = rs.l_round[t][par][lrow];
+      float l_round = rs.l_round[t][par][lrow];
       if (!warp_wait(&b.o_full[t], c & 1, p, b)) goto fail;
       tc_fence_after_sync();
       const uint32_t tO = tmem + lane_base + (t == 0 ? kColO0 : kColO1);
+      if constexpr (Cfg<HD, BN>::ONES) {  // the PV MMA's ones columns: sum of the bf16 P
+        uint32_t ls[16];
+        tmem_ld_x16(tO + HD, ls);
+        tmem_wait_ld(ls);
+        l_round = __uint_as_float(ls[0]);
+      }
       const int row = it.row0 + t * kBlockM + lrow;
       const bool store = row < p.N;
       const float inv_l = 1.f / l_round;
@@ -361,7 +371,7 @@ __global__ void __launch_bounds__(kThreadsR, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + C::SMEM_Q;
-  uint8_t* sScratch = sRing + C::NSLOT * C::KV_TILE_BYTES;  // split launches: epilogue store blocks
+  uint8_t* sScratch = sRing + C::NSLOT * C::KV_TILE_BYTES + C::ONES_BYTES;  // split launches: epilogue store blocks
   __shared__ Barriers b;
   __shared__ RowStats rs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,6 +394,12 @@ __global__ void __launch_bounds__(kThreadsR, 1)
       mbar_init(&b.slot_empty[s], 1);
     }
     fence_barrier_init();
+  }
+  if constexpr (C::ONES) {  // bf16 1.0 everywhere in the ones block, seen by the tensor core
+    uint4* ones = reinterpret_cast<uint4*>(sRing + C::NSLOT * C::KV_TILE_BYTES);
+    for (int i = threadIdx.x; i < C::ONES_BYTES / 16; i += kThreadsR)
+      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   if (warp == kMmaWarpR) {
     tmem_alloc(&b.tmem_base, kTmemCols);
