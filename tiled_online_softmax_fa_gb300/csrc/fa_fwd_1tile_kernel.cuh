@@ -21,7 +21,9 @@
 //     of the key columns, exchanging maxima and sums through shared memory), 8 MMA
 //     issuer, 9 TMA producer.  Every wait is bounded and sleeps.  Warps signal the
 //     barriers with one arrival each (lane 0 after __syncwarp); the sum of the rounded
-//     P is taken after P has been handed to the MMA.
+//     P is taken after P has been handed to the MMA, or, at head dims up to 64, by the
+//     PV MMA itself through a 16-column block of bf16 ones after the ring (O's column
+//     HD; TMEM has room beside O there).
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -44,7 +46,12 @@ struct Cfg1 {
   using C = Cfg<HD>;
   static constexpr int QBUF = HD == 256 ? 1 : 2;
   static constexpr int NSLOT = HD == 256 ? 2 : HD == 128 ? 4 : 8;
-  static constexpr int SMEM_BYTES = (QBUF + NSLOT) * C::TILE_BYTES + 1024;
+  // head dims up to 64: the PV MMA's 16 extra output columns read a block of bf16 ones
+  // placed after the ring (as in the two-tile kernel), so O's column HD holds the row sum
+  // of the rounded P
+  static constexpr bool ONES = C::ONES;
+  static constexpr int ONES_BYTES = ONES ? C::KV_CHUNK_BYTES : 0;
+  static constexpr int SMEM_BYTES = (QBUF + NSLOT) * C::TILE_BYTES + ONES_BYTES + 1024;
 };
 
 struct Barriers1 {
@@ -289,7 +296,8 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
       if (!wait1w<WARP>(&b.p_full[sb], p_cnt & 1, p, b)) goto fail;
       ++p_cnt;
       tc_fence_after_sync();
-      issue_pv<HD, kBlockN, WARP>(tmem + kColO_1, tmem + colS, ring_addr + vs * C::TILE_BYTES, j > 0);
+      issue_pv<HD, kBlockN, WARP>(tmem + kColO_1, tmem + colS, ring_addr + vs * C::TILE_BYTES, j > 0,
+                                  Cfg1<HD>::ONES ? ring_addr + NS * C::TILE_BYTES : 0u);
       mma_commit<WARP>(&b.pv_done);
       if (j == n - 1) mma_commit<WARP>(&b.o_full);
       mma_commit<WARP>(&b.slot_empty[vs]);
@@ -383,7 +391,7 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
         if (!warp_wait1(&b.pv_done, (pv_cnt - 1) & 1, p, b)) goto fail;
         tc_fence_after_sync();
 #pragma unroll
-        for (int c0 = 32 * h; c0 < HD; c0 += 64) {
+        for (int c0 = 32 * h; c0 < Cfg<HD>::NO; c0 += 64) {  // with the ones columns
           uint32_t o[32];
           tmem_ld_x32(tO + c0, o);
           tmem_wait_ld(o);
@@ -397,7 +405,7 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.p_full[sb]);
       // off the critical path: the MMA already has P
-      l_round += rounded_sum32(pk);
+      if constexpr (!Cfg1<HD>::ONES) l_round += rounded_sum32(pk);
     }
     // epilogue: O = acc / l_round in bf16, lse = (m_ref + log2 l_exact) ln 2
     x.sum[h][0][lrow] = l_exact;
@@ -411,6 +419,12 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
     if (!warp_wait1(&b.o_full, o_cnt & 1, p, b)) goto fail;
     ++o_cnt;
     tc_fence_after_sync();
+    if constexpr (Cfg1<HD>::ONES) {  // the PV MMA's ones columns: the row sum of the rounded P
+      uint32_t ls[16];
+      tmem_ld_x16(tO + HD, ls);
+      tmem_wait_ld(ls);
+      l_round = __uint_as_float(ls[0]);
+    }
     if constexpr (SPLIT) {
       // this piece's normalised partial output (fp32) and the lse of its scores
       const float inv_l = 1.f / l_round;
@@ -498,6 +512,12 @@ __global__ void __launch_bounds__(kThreads1, 1)
       mbar_init(&b.slot_empty[s], 1);
     }
     fence_barrier_init();
+  }
+  if constexpr (Cfg1<HD>::ONES) {  // bf16 1.0 everywhere in the ones block, seen by the tensor core
+    uint4* ones = reinterpret_cast<uint4*>(sRing + NS * C::TILE_BYTES);
+    for (int i = threadIdx.x; i < Cfg1<HD>::ONES_BYTES / 16; i += kThreads1)
+      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   if (warp == kMmaWarp1) {
     tmem_alloc(&b.tmem_base, kTmemCols);

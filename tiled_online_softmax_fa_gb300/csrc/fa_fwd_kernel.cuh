@@ -229,6 +229,18 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* ptr) {
   return reinterpret_cast<uint8_t*>((a + 1023) & ~uintptr_t(1023));
 }
 
+// The next item after round k that this CTA takes and that has work (k advances).
+template <bool SPLIT, int BN>
+__device__ __forceinline__ bool next_item(int& k, const Params& p, Item& it, int& u) {
+  while (++k < p.num_rounds) {
+    u = item_of(k, p);
+    if (u < 0) continue;
+    item_coords<SPLIT, BN>(u, p, it);
+    if (it.k1 > it.k0) return true;  // not an empty KV range (more splits than tiles)
+  }
+  return false;
+}
+
 // ------------------------------------------------------------------------------------
 // TMA producer (one lane)
 // ------------------------------------------------------------------------------------
@@ -325,12 +337,14 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
   const uint32_t q_addr[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE_BYTES)};
   const uint32_t col_s[2] = {kColS0, kColS1}, col_o[2] = {kColO0, kColO1};
   const uint32_t ring_addr = smem_u32(sRing);
-  for (int k = 0; k < p.num_rounds; ++k) {
-    const int u = item_of(k, p);
-    if (u < 0) continue;
-    Item it;
-    item_coords<SPLIT, BN>(u, p, it);
-    if (it.k1 <= it.k0) continue;
+  // The next item is decoded (item_of, item_coords: a handful of integer divisions) right
+  // after this item's first S MMAs are issued, while the issuer would otherwise wait for
+  // the first P; decoded at the boundary it delayed the next item's first MMAs.
+  int k_nxt = -1, u_nxt = -1;
+  Item nxt;
+  bool has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
+  while (has_nxt) {
+    const Item it = nxt;
     const int k0 = it.k0, k1 = it.k1;
     if (!warp_wait(&b.q_full, units & 1, p, b)) goto fail;
     ++units;
@@ -345,6 +359,7 @@ __device__ void mma_role(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers& b
       }
     mma_commit(&b.slot_empty[ks]);
     if (k1 - k0 == 1) mma_commit(&b.q_empty);
+    has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
     for (int j = k0; j < k1; ++j) {
       const uint32_t vs = ring % C::NSLOT;
       if (!warp_wait(&b.slot_full[vs], (ring / C::NSLOT) & 1, p, b)) goto fail;

@@ -137,13 +137,21 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
   const float c = p.scale_log2;
   const uint64_t c2 = f32x2(c, c);
   uint32_t s_cnt = 0, u_cnt = 0;
-  for (int k = 0; k < p.num_rounds; ++k) {
-    const int u = item_of(k, p);
-    if (u < 0) continue;
-    Item it;
-    item_coords<SPLIT, BN>(u, p, it);
+  // At head dim 128 the next item is decoded after this item's first P is handed over,
+  // when the next S is far off, so the boundary does not wait for it (+1.2 % at the
+  // headline); at smaller head dims the step is short and decoding there cost 3-4 %, so
+  // they decode at the boundary.
+  constexpr bool kEarlyDecode = HD >= 128;
+  int k_nxt = -1, u_nxt = -1;
+  Item nxt;
+  bool has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
+  while (has_nxt) {
+    const Item it = nxt;
     const int e_t = it.end(t);
-    if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
+    if (e_t <= it.k0 || !kEarlyDecode) {
+      has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
+      if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
+    }
     const int row = it.row0 + t * kBlockM + lrow;
     // admissible keys for this row: j <= last_key
     const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
@@ -199,6 +207,7 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.p_full[t]);
       // off the critical path: the MMA already has P, the next S is not ready yet
+      if (kEarlyDecode && j == it.k0) has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
       if constexpr (!Cfg<HD, BN>::ONES) l_round += rounded_sum(pk);
     }
     {
