@@ -137,21 +137,25 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
   const float c = p.scale_log2;
   const uint64_t c2 = f32x2(c, c);
   uint32_t s_cnt = 0, u_cnt = 0;
-  // At head dim 128 the next item is decoded after this item's first P is handed over,
-  // when the next S is far off, so the boundary does not wait for it (+1.2 % at the
-  // headline); at smaller head dims the step is short and decoding there cost 3-4 %, so
-  // they decode at the boundary.
-  constexpr bool kEarlyDecode = HD >= 128;
-  int k_nxt = -1, u_nxt = -1;
-  Item nxt;
-  bool has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
-  while (has_nxt) {
-    const Item it = nxt;
-    const int e_t = it.end(t);
-    if (e_t <= it.k0 || !kEarlyDecode) {
-      has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
-      if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
+  // At head dim 128 (unsplit) the next item is decoded after this item's first P is
+  // handed over, when the next S is far off, so the boundary does not wait for it (+1.2 %
+  // at the headline); at smaller head dims, where a step is short, and in split launches,
+  // whose items are short, decoding there cost 2-4 %, so they decode at the boundary.
+  // k_pre / pre: the round and item found ahead.
+  constexpr bool kEarlyDecode = HD >= 128 && !SPLIT;
+  int k_pre = -1;
+  Item pre;
+  for (int k = 0; k < p.num_rounds; ++k) {
+    Item it;
+    if (kEarlyDecode && k == k_pre) {
+      it = pre;
+    } else {
+      const int u = item_of(k, p);
+      if (u < 0) continue;
+      item_coords<SPLIT, BN>(u, p, it);
     }
+    const int e_t = it.end(t);
+    if (e_t <= it.k0) continue;  // this Q tile has no key tile in the item
     const int row = it.row0 + t * kBlockM + lrow;
     // admissible keys for this row: j <= last_key
     const int last_key = p.causal ? (row < p.N - 1 ? row : p.N - 1) : p.N - 1;
@@ -207,7 +211,11 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.p_full[t]);
       // off the critical path: the MMA already has P, the next S is not ready yet
-      if (kEarlyDecode && j == it.k0) has_nxt = next_item<SPLIT, BN>(k_nxt, p, nxt, u_nxt);
+      if (kEarlyDecode && j == it.k0) {
+        int kk = k, u_pre;
+        if (!next_item<SPLIT, BN>(kk, p, pre, u_pre)) kk = p.num_rounds;
+        k_pre = kk;
+      }
       if constexpr (!Cfg<HD, BN>::ONES) l_round += rounded_sum(pk);
     }
     {
@@ -221,6 +229,7 @@ __device__ void softmax_row_role(uint32_t tmem, Barriers& b, RowStats& rs, const
       if (lane == 0) mbar_arrive(&b.stats_full[t][par]);
       ++u_cnt;
     }
+    if (kEarlyDecode) k = k_pre - 1;  // the rounds before k_pre hold no work
   }
   return;
 fail:
