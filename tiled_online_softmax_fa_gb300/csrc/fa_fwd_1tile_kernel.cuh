@@ -99,6 +99,19 @@ __device__ __forceinline__ void item_coords1(int w, const Params& p, int& bh, in
   k1 = SPLIT ? (sp + 1) * n / p.splits : n;
 }
 
+// The next item after round k that this CTA takes and that has work (k advances).
+template <bool SPLIT>
+__device__ __forceinline__ bool next_item1(int& k, const Params& p, int& bh, int& row0, int& k0,
+                                           int& k1) {
+  while (++k < p.num_rounds) {
+    const int u = item_of(k, p);
+    if (u < 0) continue;
+    item_coords1<SPLIT>(u, p, bh, row0, k0, k1);
+    if (k1 > k0) return true;
+  }
+  return false;
+}
+
 // ------------------------------------------------------------------------------------
 // half-row softmax helpers: each query row is shared by two threads, one per 64-column
 // half of a 128-key score tile
@@ -260,12 +273,11 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
   uint32_t ring = 0, units = 0, oe_cnt = 0;
   uint32_t p_cnt0 = 0, p_cnt1 = 0;  // p_full completions seen, per S buffer
   const uint32_t ring_addr = smem_u32(sRing);
-  for (int k = 0; k < p.num_rounds; ++k) {
-    const int u = item_of(k, p);
-    if (u < 0) continue;
-    int bh, row0, k0, k1;
-    item_coords1<SPLIT>(u, p, bh, row0, k0, k1);
-    if (k1 <= k0) continue;
+  // the next item is decoded after this item's first S MMAs are issued, off the boundary
+  int k_nxt = -1, nbh, nrow0, nk0, nk1;
+  bool has_nxt = next_item1<SPLIT>(k_nxt, p, nbh, nrow0, nk0, nk1);
+  while (has_nxt) {
+    const int k0 = nk0, k1 = nk1;
     const int n = k1 - k0;  // key tiles of this item; tile j of the loops is k0 + j
     const uint32_t qb = units % QB;
     const uint32_t q_addr = smem_u32(sQ + qb * C::TILE_BYTES);
@@ -282,6 +294,7 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
       mma_commit<WARP>(&b.slot_empty[ks]);
     }
     if (n <= 2) mma_commit<WARP>(&b.q_empty[qb]);  // every S MMA of the unit is issued
+    has_nxt = next_item1<SPLIT>(k_nxt, p, nbh, nrow0, nk0, nk1);
     for (int j = 0; j < n; ++j) {
       const int sb = j & 1;
       const uint32_t colS = sb == 0 ? kColS0_1 : kColS1_1;
