@@ -13,17 +13,18 @@
 //     S buffer j % 2; S(j+2) reuses it only after PV(j) (MMAs of one thread run in
 //     order).  An O rescale first waits for PV(j-1) through a per-PV barrier.
 //   * Shared memory, filled by TMA with the 128-byte swizzle: at head dim 256 one
-//     64 KB Q tile and a 2-slot ring of 64 KB K/V tiles; at head dim 128 two 32 KB Q
-//     buffers (the next unit's Q loads during this one) and a 4-slot ring of 32 KB
-//     K/V tiles (both 192 KB + 1 KB alignment); at 64 and 32 two Q buffers and an
-//     8-slot ring (160 KB and 80 KB).
+//     64 KB Q tile and a 2-slot ring of 64 KB K/V tiles (192 KB + 1 KB alignment); at
+//     head dim 128 two 32 KB Q buffers (the next unit's Q loads during this one) and a
+//     3-slot ring of 32 KB K/V tiles, each followed by a 16 KB block of bf16 ones
+//     (208 KB); at 64 and 32 two Q buffers, an 8-slot ring and one ones block (176 KB
+//     and 88 KB).
 //   * Warps (384 threads): 0-7 softmax (each row shared by two threads, one per half
 //     of the key columns, exchanging maxima and sums through shared memory), 8 MMA
 //     issuer, 9 TMA producer.  Every wait is bounded and sleeps.  Warps signal the
 //     barriers with one arrival each (lane 0 after __syncwarp); the sum of the rounded
-//     P is taken after P has been handed to the MMA, or, at head dims up to 64, by the
-//     PV MMA itself through a 16-column block of bf16 ones after the ring (O's column
-//     HD; TMEM has room beside O there).
+//     P is taken by the PV MMA itself at head dims up to 128: 16 more output columns
+//     read a block of bf16 ones (O's column HD; TMEM has room beside O there); at 256 it
+//     is summed from P after P has been handed to the MMA.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -45,13 +46,18 @@ struct Cfg1 {
                 "the one-tile layout serves head dims 32 to 256");
   using C = Cfg<HD>;
   static constexpr int QBUF = HD == 256 ? 1 : 2;
-  static constexpr int NSLOT = HD == 256 ? 2 : HD == 128 ? 4 : 8;
+  static constexpr int NSLOT = HD == 256 ? 2 : HD == 128 ? 3 : 8;
   // head dims up to 64: the PV MMA's 16 extra output columns read a block of bf16 ones
   // placed after the ring (as in the two-tile kernel), so O's column HD holds the row sum
   // of the rounded P
-  static constexpr bool ONES = C::ONES;
-  static constexpr int ONES_BYTES = ONES ? C::KV_CHUNK_BYTES : 0;
-  static constexpr int SMEM_BYTES = (QBUF + NSLOT) * C::TILE_BYTES + ONES_BYTES + 1024;
+  // (at head dim 128 every ring slot carries its own 16 KB ones block right after the tile,
+  // where the descriptor's regular chunk stride puts B's third column chunk)
+  static constexpr bool ONES = HD <= 128;
+  static constexpr int NO = ONES ? HD + 16 : HD;  // PV MMA output columns
+  static constexpr int SLOT_BYTES = C::TILE_BYTES + (HD == 128 ? C::KV_CHUNK_BYTES : 0);
+  static constexpr int ONES_BYTES = (ONES && HD < 128) ? C::KV_CHUNK_BYTES : 0;  // after the ring
+  static constexpr int SMEM_BYTES = QBUF * C::TILE_BYTES + NSLOT * SLOT_BYTES + ONES_BYTES + 1024;
+  static constexpr uint32_t IDESC_O = idesc_bf16_f32(kBlockM, NO, true);
 };
 
 struct Barriers1 {
@@ -213,7 +219,7 @@ __device__ __forceinline__ bool emit_kv1(const CUtensorMap* tm, int tile, int bh
   } else {
     mbar_arrive_expect_tx(&b.slot_full[slot], C::TILE_BYTES);
     for (int c = 0; c < C::NCH; ++c)
-      tma_load_3d(sRing + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, tm, &b.slot_full[slot],
+      tma_load_3d(sRing + slot * Cfg1<HD>::SLOT_BYTES + c * C::CHUNK_BYTES, tm, &b.slot_full[slot],
                   c * C::W, tile * kBlockN, bh);
   }
   ++rs.ring;
@@ -261,6 +267,22 @@ drain:
     drain_bar(&b.q_full[i % QB], (i / QB) & 1, p);
 }
 
+// O (+ the 16 ones columns) += P V for the one-tile kernel.  Up to head dim 64 V's one
+// column chunk is followed, at the descriptor's chunk stride (ones_addr - v_addr), by the
+// ones block after the ring; at 128 each slot carries its ones block right after the
+// tile, where the regular chunk stride puts B's third chunk.  At 256: plain O += P V.
+template <int HD, bool WARP>
+__device__ __forceinline__ void issue_pv1(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
+                                          bool accumulate, uint32_t ones_addr) {
+  using C = Cfg<HD>;
+  const uint32_t lbo = (Cfg1<HD>::ONES && C::NCH == 1) ? ones_addr - v_addr : C::KV_CHUNK_BYTES;
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+    const uint64_t bd = smem_desc(v_addr + kk * 16 * C::SWB, lbo, 8 * C::SWB, C::SWZ);
+    mma_bf16_ts<WARP>(tmem_o, tmem_p + kk * 8, bd, Cfg1<HD>::IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // MMA issuer (one lane)
 // ------------------------------------------------------------------------------------
@@ -289,7 +311,7 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
       if (!wait1w<WARP>(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
       ++ring;
       tc_fence_after_sync();
-      issue_s<HD, kBlockN, WARP>(tmem + (j == 0 ? kColS0_1 : kColS1_1), q_addr, ring_addr + ks * C::TILE_BYTES);
+      issue_s<HD, kBlockN, WARP>(tmem + (j == 0 ? kColS0_1 : kColS1_1), q_addr, ring_addr + ks * Cfg1<HD>::SLOT_BYTES);
       mma_commit<WARP>(&b.s_full[j]);
       mma_commit<WARP>(&b.slot_empty[ks]);
     }
@@ -309,8 +331,8 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
       if (!wait1w<WARP>(&b.p_full[sb], p_cnt & 1, p, b)) goto fail;
       ++p_cnt;
       tc_fence_after_sync();
-      issue_pv<HD, kBlockN, WARP>(tmem + kColO_1, tmem + colS, ring_addr + vs * C::TILE_BYTES, j > 0,
-                                  Cfg1<HD>::ONES ? ring_addr + NS * C::TILE_BYTES : 0u);
+      issue_pv1<HD, WARP>(tmem + kColO_1, tmem + colS, ring_addr + vs * Cfg1<HD>::SLOT_BYTES, j > 0,
+                          ring_addr + NS * Cfg1<HD>::SLOT_BYTES);
       mma_commit<WARP>(&b.pv_done);
       if (j == n - 1) mma_commit<WARP>(&b.o_full);
       mma_commit<WARP>(&b.slot_empty[vs]);
@@ -319,7 +341,7 @@ __device__ void mma_role1(uint8_t* sQ, uint8_t* sRing, uint32_t tmem, Barriers1&
         if (!wait1w<WARP>(&b.slot_full[ks], (ring / NS) & 1, p, b)) goto fail;
         ++ring;
         tc_fence_after_sync();
-        issue_s<HD, kBlockN, WARP>(tmem + colS, q_addr, ring_addr + ks * C::TILE_BYTES);
+        issue_s<HD, kBlockN, WARP>(tmem + colS, q_addr, ring_addr + ks * Cfg1<HD>::SLOT_BYTES);
         mma_commit<WARP>(&b.s_full[sb]);
         mma_commit<WARP>(&b.slot_empty[ks]);
         if (j + 2 == n - 1) mma_commit<WARP>(&b.q_empty[qb]);
@@ -404,7 +426,7 @@ __device__ void softmax_role1(uint32_t tmem, Barriers1& b, Xchg1& x, const Param
         if (!warp_wait1(&b.pv_done, (pv_cnt - 1) & 1, p, b)) goto fail;
         tc_fence_after_sync();
 #pragma unroll
-        for (int c0 = 32 * h; c0 < Cfg<HD>::NO; c0 += 64) {  // with the ones columns
+        for (int c0 = 32 * h; c0 < Cfg1<HD>::NO; c0 += 64) {  // with the ones columns
           uint32_t o[32];
           tmem_ld_x32(tO + c0, o);
           tmem_wait_ld(o);
@@ -526,10 +548,15 @@ __global__ void __launch_bounds__(kThreads1, 1)
     }
     fence_barrier_init();
   }
-  if constexpr (Cfg1<HD>::ONES) {  // bf16 1.0 everywhere in the ones block, seen by the tensor core
-    uint4* ones = reinterpret_cast<uint4*>(sRing + NS * C::TILE_BYTES);
-    for (int i = threadIdx.x; i < Cfg1<HD>::ONES_BYTES / 16; i += kThreads1)
-      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  if constexpr (Cfg1<HD>::ONES) {  // bf16 1.0 everywhere in the ones blocks, seen by the tensor core
+    constexpr int OB = HD == 128 ? C::KV_CHUNK_BYTES : Cfg1<HD>::ONES_BYTES;  // bytes per block
+    constexpr int NB = HD == 128 ? NS : 1;                                     // blocks
+    for (int i = threadIdx.x; i < NB * OB / 16; i += kThreads1) {
+      const int blk = i / (OB / 16), off = i % (OB / 16);
+      uint8_t* base = HD == 128 ? sRing + blk * Cfg1<HD>::SLOT_BYTES + C::TILE_BYTES
+                                : sRing + NS * Cfg1<HD>::SLOT_BYTES;
+      reinterpret_cast<uint4*>(base)[off] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    }
     fence_proxy_async_smem();
   }
   if (warp == kMmaWarp1) {
