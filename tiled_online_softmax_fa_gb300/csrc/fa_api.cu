@@ -183,15 +183,14 @@ struct CostModel {
   double merge_per_mb;  // per MB of fp32 partial outputs (written, merged)
   double one_piece;     // fixed cost of a one-tile split piece, in one-tile steps
 };
-// Fitted to GB300 timings.  Unit and step costs: per head dim, the two-tile and one-tile
-// kernels timed on 44 shapes (B 1-2, H 1-64, N 256-65536, causal and not), the three
-// constants chosen on a grid to minimise the time lost to wrong picks: the model's pick
-// is within 2 % of the faster kernel on 43 of 44 shapes at d = 128 (the other 6 %), and on
-// all 44 at d = 64 and 32.
-// Split costs: one to eight heads at N = 4096-32768 (16 shapes per head dim), each timed
-// on both kernels unsplit and split 2-8 ways; the model's pick is within 0.1 % of the
-// measured best at d = 32, 64 and 256 and within 8 % at d = 128 (one 406-vs-438 TFLOP/s
-// shape; 0 elsewhere).  At d = 256 only the one-tile kernel runs: its step is the unit.
+// Fitted to GB300 timings of the current kernels, per head dim: both kernels unsplit on
+// 46 shapes (B*H 1-64, N 256-65536, causal and not) and split 2, 3, 4, 5, 6 and 8 ways on
+// the 21 of them with at most 152 two-tile or 304 one-tile units (d = 256: the one-tile
+// kernel on 16 shapes).  The constants were chosen on a grid to minimise the time lost to
+// wrong picks, replaying this planner exactly: its pick is within 2 % of the fastest
+// measured launch on 45 of 46 shapes at d = 128 (the other 2.2 %), all 46 at d = 64, 45
+// of 46 at d = 32 (the other 5.9 %) and 15 of 16 at d = 256 (2.6 %).  At d = 256 only
+// the one-tile kernel runs: its step is the unit.
 constexpr CostModel kCostD128 = {3.0, 1.0, 1.07, 6.0, 10.0, 0.25, 4.0};
 constexpr CostModel kCostD64 = {8.0, 2.0, 1.30, 8.0, 15.0, 0.25, 1.0};
 constexpr CostModel kCostD32 = {8.0, 2.0, 1.30, 4.0, 20.0, 0.25, 1.0};
