@@ -41,6 +41,7 @@ import workloads  # noqa: E402
 METRIC = "FA fwd TFLOP/s (causal 2BHN²d) at b8 h32 S8192 d128 bf16; % of GB300 BF16 peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
+SUSTAINED_S = 0.5  # timed regions this long run at the power cap: the sustained peak applies
 # The device code of the kernel the bench line times (head dims 16-128): an ncu traffic
 # record applies only while these files are unchanged.
 SOURCES = ["tiled_online_softmax_fa_gb300/csrc/fa_fwd_kernel.cuh",
@@ -75,13 +76,20 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def load_peaks():
+def load_peaks(timed_s=0.0):
+    """The bf16 peak for a roofline fraction: the burst figure for a kernel timed alone,
+    the sustained one (a seconds-long loop under the power cap) once the timed region
+    lasts SUSTAINED_S or more."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             pk = json.load(f)
+        if timed_s >= SUSTAINED_S and pk.get("bf16_tflops_sustained"):
+            return (float(pk["bf16_tflops_sustained"]),
+                    f"measured (MEASURED_PEAKS.json bf16_tflops_sustained: timed region {timed_s:.2f} s)")
         if pk.get("bf16_tflops"):
-            return float(pk["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+            return (float(pk["bf16_tflops"]),
+                    f"measured (MEASURED_PEAKS.json bf16_tflops, burst: timed region {timed_s:.2f} s)")
     return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
 
 
@@ -563,7 +571,7 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return 0
 
-    peak, peak_src = load_peaks()
+    peak, peak_src = load_peaks(ms_step * args.steps * 1e-3)
     traffic, traffic_note = None, "no ncu capture matching this kernel source"
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:

@@ -83,3 +83,20 @@ def test_page_traffic_models_match_the_page():
         assert round(m["qkvo_bytes"] / 1e6, 2) == r["qkvo_compulsory_bytes_mb"]
         assert round(m["materialised_bytes"] / 1e6, 2) == r["standard_total_hbm_mb"]
         assert round(m["tiled_no_reuse_bytes"] / 1e6, 2) == r["tiled_logical_access_mb_no_cache_reuse"]
+
+
+def test_peak_follows_the_timed_region():
+    """A timed region shorter than bench.SUSTAINED_S is measured against the burst bf16
+    peak, a longer one (at the power cap) against the sustained peak, when the driver's
+    measurements hold both."""
+    path = os.path.join(bench.ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        pytest.skip("no MEASURED_PEAKS.json")
+    with open(path) as f:
+        pk = json.load(f)
+    if not pk.get("bf16_tflops") or not pk.get("bf16_tflops_sustained"):
+        pytest.skip("MEASURED_PEAKS.json lacks a bf16 figure")
+    short, src_short = bench.load_peaks(0.05)
+    long_, src_long = bench.load_peaks(bench.SUSTAINED_S + 0.5)
+    assert short == pytest.approx(pk["bf16_tflops"]) and "burst" in src_short
+    assert long_ == pytest.approx(pk["bf16_tflops_sustained"]) and "sustained" in src_long
