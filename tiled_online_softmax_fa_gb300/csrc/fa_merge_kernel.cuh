@@ -38,7 +38,7 @@ __device__ __forceinline__ void load_partial(const float* src, float (&x)[E]) {
 // The merge of one query row, in two halves so that a warp can put the loads of several
 // rows in flight before it needs any of them (merge_load, then merge_finish).
 struct MergeRow {
-  int bh, row, rin, t;
+  int bh, row, rin, t, qb;
   size_t base;  // the row's first piece (item index)
   bool valid;   // row < BH * N
 };
@@ -46,11 +46,18 @@ struct MergeRow {
 template <int UNIT_ROWS>
 __device__ __forceinline__ MergeRow merge_row(const Params& p, int64_t gw) {
   MergeRow r;
-  r.valid = gw < static_cast<int64_t>(p.BH) * p.N;
+  const int64_t rows = static_cast<int64_t>(p.BH) * p.N;
+  r.valid = gw < rows;
   if (!r.valid) gw = 0;
-  r.bh = static_cast<int>(gw / p.N);
-  r.row = static_cast<int>(gw - static_cast<int64_t>(r.bh) * p.N);
+  if (rows <= 0x7FFFFFFF) {  // 32-bit division where the row count allows (a 64-bit one is a call)
+    r.bh = static_cast<int>(static_cast<uint32_t>(gw) / static_cast<uint32_t>(p.N));
+    r.row = static_cast<int>(gw) - r.bh * p.N;
+  } else {
+    r.bh = static_cast<int>(gw / p.N);
+    r.row = static_cast<int>(gw - static_cast<int64_t>(r.bh) * p.N);
+  }
   const int qb = r.row / UNIT_ROWS;
+  r.qb = qb;
   r.rin = r.row - qb * UNIT_ROWS;
   r.t = r.rin / kBlockM;
   // unit of (bh, qb): the inverse of unit_coords
@@ -110,15 +117,19 @@ __global__ void __launch_bounds__(kMergeThreads)
     for (int h = 0; h < 2; ++h) {
       const int sp = lane + 32 * h;
       if (sp < p.splits) {
+        // piece sp of the row's unit holds an admissible key for the row's Q tile (the
+        // kernels' item_coords, from the row's query block)
         bool holds;
         if constexpr (UNIT_ROWS == kUnitRows) {
-          Item it;
-          item_coords<true, BN>(static_cast<int>(m0.base) + sp, p, it);
-          holds = it.end(m0.t) > it.k0;
+          const int row0 = m0.qb * kUnitRows;
+          const int n0 = tiles_for<BN>(row0, p), n1 = tiles_for<BN>(row0 + kBlockM, p);
+          const int n = n0 > n1 ? n0 : n1;
+          const int k0 = sp * n / p.splits, k1 = (sp + 1) * n / p.splits;
+          const int nt = m0.t == 0 ? n0 : n1;
+          holds = (nt < k1 ? nt : k1) > k0;
         } else {
-          int ibh, irow0, k0, k1;
-          one::item_coords1<true>(static_cast<int>(m0.base) + sp, p, ibh, irow0, k0, k1);
-          holds = k1 > k0;
+          const int n = tiles_for(m0.qb * one::kUnitRows1, p);
+          holds = (sp + 1) * n / p.splits > sp * n / p.splits;
         }
         if (holds) ls[h] = p.ws_lse[(m0.base + sp) * UNIT_ROWS + m0.rin];
       }
