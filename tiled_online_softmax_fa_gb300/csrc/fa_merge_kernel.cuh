@@ -4,7 +4,9 @@
 // logsumexp lse_s of its scores.  The full softmax over the union of the ranges is
 //     lse = ln sum_s exp(lse_s),    O = sum_s exp(lse_s - lse) O_s
 // (each range's weights sum to one, so exp(lse_s - lse) is that range's share of the
-// row's total probability mass).  Memory bound: one warp per row, coalesced loads.
+// row's total probability mass).  One warp per row, coalesced loads.  The kernel is as
+// much instruction- as memory-bound: the row's unit and each piece's key range come from
+// 32-bit arithmetic on the row's query block, and the weights and lse from ex2 / lg2.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -15,6 +17,7 @@
 namespace fa_sm103 {
 
 constexpr int kMergeThreads = 256;  // 8 rows per block
+constexpr float kLog2e = 1.4426950408889634f;
 
 // E consecutive fp32 values of a partial output (E = 1, 2, 4 or 8 per lane).
 template <int E>
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
     float w[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) w[h] = ls[h] == -INFINITY ? 0.f : expf(ls[h] - m);
+    for (int h = 0; h < 2; ++h) w[h] = ls[h] == -INFINITY ? 0.f : ex2_approx((ls[h] - m) * kLog2e);
     float denom = w[0] + w[1];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xFFFFFFFFu, denom, off);
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kMergeThreads)
       }
     }
     if (lane == 0 && p.lse != nullptr)
-      p.lse[static_cast<size_t>(m0.bh) * p.N + m0.row] = m + logf(denom);
+      p.lse[static_cast<size_t>(m0.bh) * p.N + m0.row] = m + lg2_approx(denom) * kLn2;
   }
 }
 
