@@ -198,4 +198,81 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
 }
 
+
+// Two-piece merge with two rows per warp (head dims up to 128): each half-warp takes one
+// row, 16 lanes x HD/16 columns, so one instruction stream serves two rows.  Otherwise
+// the same arithmetic as fa_merge_kernel with NP = 2.
+template <int HD, int UNIT_ROWS, int BN>
+__global__ void __launch_bounds__(kMergeThreads)
+    fa_merge2_kernel(const Params p) {
+  static_assert(HD <= 128, "head dims 16 to 128");
+  constexpr int E = HD / 16;  // columns per lane
+  const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5)) * 2 + half;
+  const MergeRow m0 = merge_row<UNIT_ROWS>(p, gw);
+  float x[2][E];
+#pragma unroll
+  for (int sp = 0; sp < 2; ++sp)
+    if (sp < p.splits && m0.valid)
+      load_partial<E>(p.ws_o + ((m0.base + sp) * UNIT_ROWS + m0.rin) * HD + hl * E, x[sp]);
+  // piece hl (lanes 0 and 1 of the half): its lse, or -inf without an admissible key
+  float ls = -INFINITY;
+  if (hl < p.splits && m0.valid) {
+    bool holds;
+    if constexpr (UNIT_ROWS == kUnitRows) {
+      const int row0 = m0.qb * kUnitRows;
+      const int n0 = tiles_for<BN>(row0, p), n1 = tiles_for<BN>(row0 + kBlockM, p);
+      const int n = n0 > n1 ? n0 : n1;
+      const int k0 = hl * n / p.splits, k1 = (hl + 1) * n / p.splits;
+      const int nt = m0.t == 0 ? n0 : n1;
+      holds = (nt < k1 ? nt : k1) > k0;
+    } else {
+      const int n = tiles_for(m0.qb * one::kUnitRows1, p);
+      holds = (hl + 1) * n / p.splits > hl * n / p.splits;
+    }
+    if (holds) ls = p.ws_lse[(m0.base + hl) * UNIT_ROWS + m0.rin];
+  }
+  float mx = ls;
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  float w = ls == -INFINITY ? 0.f : ex2_approx((ls - mx) * kLog2e);
+  float denom = w;
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) denom += __shfl_xor_sync(0xFFFFFFFFu, denom, off);
+  const float w0 = __shfl_sync(0xFFFFFFFFu, w, half * 16), w1 = __shfl_sync(0xFFFFFFFFu, w, half * 16 + 1);
+  if (!m0.valid) return;
+  float acc[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) acc[i] = 0.f;
+  if (w0 != 0.f) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] += w0 * x[0][i];
+  }
+  if (w1 != 0.f) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] += w1 * x[1][i];
+  }
+  const float inv = 1.f / denom;
+  __nv_bfloat16* dst = p.o + (static_cast<size_t>(m0.bh) * p.N + m0.row) * HD + hl * E;
+  if constexpr (E == 8) {
+    uint4 v;
+    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(dst) = v;
+  } else if constexpr (E == 4) {
+    uint2 v;
+    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = v;
+  } else if constexpr (E == 2) {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  } else {
+    dst[0] = __float2bfloat16_rn(acc[0] * inv);
+  }
+  if (hl == 0 && p.lse != nullptr)
+    p.lse[static_cast<size_t>(m0.bh) * p.N + m0.row] = mx + lg2_approx(denom) * kLn2;
+}
+
 }  // namespace fa_sm103
