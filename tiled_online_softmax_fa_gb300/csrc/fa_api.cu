@@ -496,10 +496,15 @@ int launch_merge(const fa_sm103::Params& p, int64_t BH, int64_t N, cudaStream_t 
   auto blocks = [&](int rows_per_warp) {
     return static_cast<unsigned>((rows + int64_t{WPB} * rows_per_warp - 1) / (int64_t{WPB} * rows_per_warp));
   };
-  // two pieces at head dims up to 128: a half-warp per row (65,536 rows: 19.5 -> 13.8 us)
+  // up to four pieces at head dims up to 128: a half-warp per row (65,536 rows x 2 pieces:
+  // 19.5 -> 13.8 us; x 4: 16.4 -> 13.4 us); with 5-8 pieces the partials held per lane make
+  // it slower than a warp per row
   if constexpr (HD <= 128) {
-    if (p.splits <= 2) {
-      fa_sm103::fa_merge2_kernel<HD, UNIT_ROWS, BN><<<blocks(2), T, 0, stream>>>(p);
+    if (p.splits <= 4) {
+      if (p.splits <= 2)
+        fa_sm103::fa_merge2_kernel<HD, UNIT_ROWS, BN, 2><<<blocks(2), T, 0, stream>>>(p);
+      else
+        fa_sm103::fa_merge2_kernel<HD, UNIT_ROWS, BN, 4><<<blocks(2), T, 0, stream>>>(p);
       const cudaError_t e = cudaGetLastError();
       return e != cudaSuccess ? cuda_error("merge kernel launch", e) : FA_OK;
     }

@@ -199,10 +199,10 @@ __global__ void __launch_bounds__(kMergeThreads)
 }
 
 
-// Two-piece merge with two rows per warp (head dims up to 128): each half-warp takes one
-// row, 16 lanes x HD/16 columns, so one instruction stream serves two rows.  Otherwise
-// the same arithmetic as fa_merge_kernel with NP = 2.
-template <int HD, int UNIT_ROWS, int BN>
+// Merge of up to NP pieces with two rows per warp (head dims up to 128): each half-warp
+// takes one row, 16 lanes x HD/16 columns, so one instruction stream serves two rows.
+// Otherwise the same arithmetic as fa_merge_kernel with NP up-front pieces.
+template <int HD, int UNIT_ROWS, int BN, int NP = 2>
 __global__ void __launch_bounds__(kMergeThreads)
     fa_merge2_kernel(const Params p) {
   static_assert(HD <= 128, "head dims 16 to 128");
@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5)) * 2 + half;
   const MergeRow m0 = merge_row<UNIT_ROWS>(p, gw);
-  float x[2][E];
+  float x[NP][E];
 #pragma unroll
-  for (int sp = 0; sp < 2; ++sp)
+  for (int sp = 0; sp < NP; ++sp)
     if (sp < p.splits && m0.valid)
       load_partial<E>(p.ws_o + ((m0.base + sp) * UNIT_ROWS + m0.rin) * HD + hl * E, x[sp]);
   // piece hl (lanes 0 and 1 of the half): its lse, or -inf without an admissible key
@@ -239,19 +239,19 @@ __global__ void __launch_bounds__(kMergeThreads)
   float denom = w;
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) denom += __shfl_xor_sync(0xFFFFFFFFu, denom, off);
-  const float w0 = __shfl_sync(0xFFFFFFFFu, w, half * 16), w1 = __shfl_sync(0xFFFFFFFFu, w, half * 16 + 1);
+  float wp[NP];
+#pragma unroll
+  for (int sp = 0; sp < NP; ++sp) wp[sp] = __shfl_sync(0xFFFFFFFFu, w, half * 16 + sp);
   if (!m0.valid) return;
   float acc[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) acc[i] = 0.f;
-  if (w0 != 0.f) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) acc[i] += w0 * x[0][i];
-  }
-  if (w1 != 0.f) {
+  for (int sp = 0; sp < NP; ++sp)
+    if (sp < p.splits && wp[sp] != 0.f) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) acc[i] += w1 * x[1][i];
-  }
+      for (int i = 0; i < E; ++i) acc[i] += wp[sp] * x[sp][i];
+    }
   const float inv = 1.f / denom;
   __nv_bfloat16* dst = p.o + (static_cast<size_t>(m0.bh) * p.N + m0.row) * HD + hl * E;
   if constexpr (E == 8) {
