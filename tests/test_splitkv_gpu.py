@@ -43,7 +43,7 @@ def test_n4k_noncausal_sampled():
 
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("N", [129, 300, 700])
-@pytest.mark.parametrize("splits", [2, 5])
+@pytest.mark.parametrize("splits", [2, 4, 5])  # the merge: a half-warp per row up to 4 pieces
 def test_ragged(d, N, splits):
     w = W["n1k"]
     rows = workloads.select_rows(w, B=2, H=3, N=N, seed=N + d)
