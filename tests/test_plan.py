@@ -6,7 +6,8 @@ units) by replaying the kernels' static schedule on a cost model.  These tests p
 to GB300 measurements: for every shape below one candidate was measured more than 2%
 faster than the others (bf16, mean of 20 launches after 3 warm-ups, CUDA events; the
 current kernels, with the row sum of the rounded P from the PV MMA and the next unit
-decoded off the unit boundary), and the planner, asked for 152 SMs, must pick it.
+decoded off the unit boundary; the d = 128 split launches with the merge kernel's
+half-warp layout), and the planner, asked for 152 SMs, must pick it.
 Candidates timed per head dim with `bench.py --d D --sweep out.json --kernel two|one
 [--noncausal] [--splits S] --sweep-shapes ...` (S = 2, 3, 4, 5, 6, 8 on the shapes with
 at most 152 two-tile or 304 one-tile units).  Near-ties (< 2%) are left out: either
@@ -27,21 +28,21 @@ TWO, ONE = fa.FA_KERNEL_TWO_TILE, fa.FA_KERNEL_ONE_TILE
 # splits were timed)
 MEASURED = {
     (1, 1, 4096, True): "one-split", (1, 1, 8192, True): "one-split",
-    (1, 1, 12288, True): "one-split", (1, 1, 24576, True): "two-split",
-    (1, 1, 32768, True): "one", (1, 1, 65536, True): "one", (1, 2, 8192, True): "one-split",
-    (1, 2, 12288, True): "two-split", (1, 2, 16384, True): "one",
-    (1, 2, 24576, True): "one", (1, 2, 32768, True): "one", (1, 3, 8192, True): "one",
-    (1, 3, 12288, True): "one", (1, 3, 16384, True): "one", (1, 4, 4096, True): "one",
-    (1, 4, 8192, False): "two", (1, 4, 8192, True): "one", (1, 4, 16384, True): "one",
-    (1, 5, 6144, True): "one", (1, 6, 6144, True): "one", (1, 6, 8192, True): "one",
-    (1, 8, 4096, False): "two", (1, 8, 4096, True): "one", (1, 10, 8192, True): "two",
-    (1, 12, 4096, True): "one", (1, 16, 1024, True): "one", (1, 16, 2048, True): "one",
-    (1, 16, 4096, False): "two", (1, 16, 4096, True): "two", (1, 24, 2048, True): "one",
-    (1, 32, 256, True): "one", (1, 32, 512, True): "one", (1, 32, 1024, False): "two",
-    (1, 32, 1024, True): "one", (1, 32, 2048, False): "two", (1, 32, 2048, True): "one",
-    (1, 32, 4096, True): "two", (1, 40, 2048, True): "two", (1, 48, 1024, True): "one",
-    (1, 48, 2048, False): "two", (1, 48, 2048, True): "one", (1, 64, 1024, True): "one",
-    (1, 64, 2048, True): "one",
+    (1, 1, 12288, True): "one-split", (1, 1, 16384, True): "one-split",
+    (1, 1, 24576, True): "two-split", (1, 1, 65536, True): "one",
+    (1, 2, 8192, True): "one-split", (1, 2, 12288, True): "two-split",
+    (1, 2, 16384, True): "one", (1, 2, 24576, True): "one", (1, 2, 32768, True): "one",
+    (1, 3, 8192, True): "one", (1, 3, 12288, True): "one", (1, 3, 16384, True): "one",
+    (1, 4, 4096, True): "one-split", (1, 4, 8192, False): "two", (1, 4, 8192, True): "one",
+    (1, 4, 16384, True): "one", (1, 5, 6144, True): "one", (1, 6, 6144, True): "one",
+    (1, 6, 8192, True): "one", (1, 8, 4096, False): "two", (1, 8, 4096, True): "one",
+    (1, 10, 8192, True): "two", (1, 12, 4096, True): "one", (1, 16, 1024, True): "one",
+    (1, 16, 2048, True): "one", (1, 16, 4096, False): "two", (1, 16, 4096, True): "two",
+    (1, 24, 2048, True): "one", (1, 32, 256, True): "one", (1, 32, 512, True): "one",
+    (1, 32, 1024, False): "two", (1, 32, 1024, True): "one", (1, 32, 2048, False): "two",
+    (1, 32, 2048, True): "one", (1, 32, 4096, True): "two", (1, 40, 2048, True): "two",
+    (1, 48, 1024, True): "one", (1, 48, 2048, False): "two", (1, 48, 2048, True): "one",
+    (1, 64, 1024, True): "one", (1, 64, 2048, True): "one",
 }
 
 MEASURED_D64 = {

@@ -189,9 +189,11 @@ struct CostModel {
 // kernel on 16 shapes).  The constants were chosen on a grid to minimise the time lost to
 // wrong picks, replaying this planner exactly: its pick is within 2 % of the fastest
 // measured launch on 45 of 46 shapes at d = 128 (the other 2.2 %), all 46 at d = 64, 45
-// of 46 at d = 32 (the other 5.9 %) and 15 of 16 at d = 256 (2.6 %).  At d = 256 only
-// the one-tile kernel runs: its step is the unit.
-constexpr CostModel kCostD128 = {3.0, 1.0, 1.07, 6.0, 10.0, 0.25, 4.0};
+// of 46 at d = 32 (the other 5.9 %) and 15 of 16 at d = 256 (2.6 %).  The split costs at
+// d = 128 were refitted once more after the merge kernel got faster (a half-warp per row
+// for up to four pieces); d = 32, 64 and 256 keep the fit to the earlier merge.  At d =
+// 256 only the one-tile kernel runs: its step is the unit.
+constexpr CostModel kCostD128 = {3.0, 1.0, 1.07, 12.0, 0.0, 0.25, 6.0};
 constexpr CostModel kCostD64 = {8.0, 2.0, 1.30, 8.0, 15.0, 0.25, 1.0};
 constexpr CostModel kCostD32 = {8.0, 2.0, 1.30, 4.0, 20.0, 0.25, 1.0};
 constexpr CostModel kCostD256 = {0.0, 0.0, 1.0, 0.0, 0.0, 0.25, 3.0};
