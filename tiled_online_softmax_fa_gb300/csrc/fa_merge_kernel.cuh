@@ -77,10 +77,11 @@ __device__ __forceinline__ MergeRow merge_row(const Params& p, int64_t gw) {
 // its E bf16 outputs with one vector store.  With at most NP pieces (NP = 2 or 8; the
 // host picks the smallest that holds the launch's split count) the partial outputs are
 // loaded before the lse values are known, so a row costs one memory round trip instead
-// of two, and the registers for them are sized to NP, so launches of few pieces keep
-// more rows in flight per SM (memory-bound: bytes in flight set the rate); NP = 0 loads
-// each piece once its weight is known.  With R = 2 a warp merges two consecutive rows,
-// all of their loads issued before either row is finished.  A piece without an
+// of two, and the registers for them are sized to NP; NP = 0 loads each piece once its
+// weight is known.  With R = 2 a warp merges two consecutive rows, all of their loads
+// issued before either row is finished (measured slower than R = 1; the host launches
+// R = 1).  At head dims up to 128 the host takes fa_merge2_kernel (below) for up to four
+// pieces and this kernel for more, or for head dim 256.  A piece without an
 // admissible key for the row (its key range starts past the row's diagonal tile, its
 // partial never written) has weight 0 and its loaded values are not used.
 // UNIT_ROWS: the query rows of the split kernel's work unit -- kUnitRows (two-tile
